@@ -1,0 +1,340 @@
+"""Pins of the attention / cache-op oracle to facts outside the oracle.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with
+a value fixed by the pages or by the mathematics.  ``test_oracle_pins.py``
+runs them; ``test_oracle_mutations.py`` runs them against deliberately
+broken copies of the oracle to show that every planted mistake fails one.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+from scipy.special import softmax
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+DT = {"float16": torch.float16, "bfloat16": torch.bfloat16}
+
+
+def to_bits(values, dtype):
+    """float values -> 16-bit patterns of the storage dtype (torch rounding)."""
+    t = torch.as_tensor(np.asarray(values, dtype=np.float32)).to(DT[dtype])
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def widen(bits, dtype):
+    """16-bit patterns -> float64 through torch (a library conversion)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(DT[dtype])
+    return t.to(torch.float64).numpy()
+
+
+def build_pool(tokens_k, tokens_v, tables, block_size, num_blocks, dtype, fill=0.0):
+    """Place per-sequence token rows [n][H][d] into pools through block tables.
+
+    Written as explicit loops over (sequence, token): logical token t sits in
+    physical block tables[s][t // B], slot t % B.
+    """
+    H, d = tokens_k[0].shape[1], tokens_k[0].shape[2]
+    kc = np.full((num_blocks, H, block_size, d), fill, dtype=np.float32)
+    vc = np.full_like(kc, fill)
+    for s, (ks, vs) in enumerate(zip(tokens_k, tokens_v)):
+        for t in range(ks.shape[0]):
+            b = tables[s][t // block_size]
+            kc[b, :, t % block_size, :] = ks[t]
+            vc[b, :, t % block_size, :] = vs[t]
+    max_blocks = max(len(t) for t in tables)
+    bt = np.zeros((len(tables), max_blocks), dtype=np.int32)
+    for s, t in enumerate(tables):
+        bt[s, :len(t)] = t
+    return to_bits(kc, dtype), to_bits(vc, dtype), bt
+
+
+def random_case(rng, lengths, H_q, H_kv, d, block_size, dtype, spare=3):
+    """Random tokens for each sequence, blocks scattered over a shuffled pool."""
+    need = [max(1, -(-n // block_size)) for n in lengths]
+    nb = sum(need) + spare
+    perm = rng.permutation(nb)
+    tables, pos = [], 0
+    for k in need:
+        tables.append([int(b) for b in perm[pos:pos + k]])
+        pos += k
+    ks = [rng.standard_normal((n, H_kv, d)).astype(np.float32) for n in lengths]
+    vs = [rng.standard_normal((n, H_kv, d)).astype(np.float32) for n in lengths]
+    kc, vc, bt = build_pool(ks, vs, tables, block_size, nb, dtype,
+                            fill=float(rng.standard_normal()))
+    q = to_bits(rng.standard_normal((len(lengths), H_q, d)), dtype)
+    return q, kc, vc, bt, np.asarray(lengths, dtype=np.int32), tables
+
+
+# ---------------------------------------------------------------------------
+# fp16 / bf16 widening
+# ---------------------------------------------------------------------------
+def pin_f16_widening_all_patterns():
+    patterns = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = patterns.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(b)) for b in patterns])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got)), "binary16 widening differs from numpy"
+    assert np.all(np.signbit(ref[~both_nan]) == np.signbit(got[~both_nan]))
+
+
+def pin_bf16_widening_all_patterns():
+    patterns = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = widen(patterns, "bfloat16")
+    got = np.array([oracle.bf16_to_f64(int(b)) for b in patterns])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got)), "bfloat16 widening differs from torch"
+
+
+# ---------------------------------------------------------------------------
+# Closed forms
+# ---------------------------------------------------------------------------
+def pin_hand_example():
+    """d = 2, scale = ln 2, two query heads sharing one KV head (GQA g = 2).
+
+    Keys (1,0), (0,0), (2,0); values (7,0), (0,7), (-7,14).
+    Head 0, q = (1,0): scores ln2 * (1, 0, 2), exp -> (2, 1, 4), weights
+    (2, 1, 4) / 7, output (14 - 28, 7 + 56) / 7 = (-2, 9).
+    Head 1, q = (0,0): equal weights, output = mean of values = (0, 7).
+    The three tokens sit in blocks of 2 at physical blocks 5 and 2.
+    """
+    for dtype in ("float16", "bfloat16"):
+        ks = [np.array([[[1, 0]], [[0, 0]], [[2, 0]]], dtype=np.float32)]
+        vs = [np.array([[[7, 0]], [[0, 7]], [[-7, 14]]], dtype=np.float32)]
+        kc, vc, bt = build_pool(ks, vs, [[5, 2]], 2, 6, dtype, fill=99.0)
+        q = to_bits([[[1, 0], [0, 0]]], dtype)
+        out = oracle.attention(q, kc, vc, bt, [3], math.log(2.0), dtype)
+        assert np.allclose(out[0, 0], [-2.0, 9.0], rtol=0, atol=1e-13), out
+        assert np.allclose(out[0, 1], [0.0, 7.0], rtol=0, atol=1e-13), out
+
+
+def pin_single_token_is_value_row():
+    rng = np.random.default_rng(1)
+    for dtype in ("float16", "bfloat16"):
+        q, kc, vc, bt, lens, tables = random_case(rng, [1, 1, 1], 4, 2, 16, 4, dtype)
+        out = oracle.attention(q, kc, vc, bt, lens, 0.25, dtype)
+        for s in range(3):
+            b = tables[s][0]
+            for i in range(4):
+                expect = widen(vc[b, i // 2, 0], dtype)
+                assert np.array_equal(out[s, i], expect), "n = 1 must return V_0 exactly"
+
+
+def pin_zero_query_is_mean_of_values():
+    rng = np.random.default_rng(2)
+    lengths = [5, 17, 33]
+    q, kc, vc, bt, lens, tables = random_case(rng, lengths, 2, 1, 8, 4, "bfloat16")
+    q = np.zeros_like(q)
+    out = oracle.attention(q, kc, vc, bt, lens, 0.3, "bfloat16")
+    for s, n in enumerate(lengths):
+        rows = np.stack([widen(vc[tables[s][t // 4], 0, t % 4], "bfloat16") for t in range(n)])
+        assert np.allclose(out[s, 0], rows.mean(axis=0), rtol=1e-13, atol=1e-14)
+
+
+def pin_equal_keys_give_mean_of_values():
+    rng = np.random.default_rng(3)
+    n, d = 11, 8
+    key = rng.standard_normal(d).astype(np.float32)
+    ks = [np.tile(key, (n, 1, 1))]
+    vs = [rng.standard_normal((n, 1, d)).astype(np.float32)]
+    kc, vc, bt = build_pool(ks, vs, [[3, 0, 2]], 4, 4, "float16")
+    q = to_bits(rng.standard_normal((1, 1, d)), "float16")
+    out = oracle.attention(q, kc, vc, bt, [n], 1.0, "float16")
+    mean = widen(to_bits(vs[0][:, 0], "float16"), "float16").mean(axis=0)
+    assert np.allclose(out[0, 0], mean, rtol=1e-13, atol=1e-14)
+
+
+def pin_extreme_logits_are_one_hot():
+    """Scores up to +-1.0e4 must neither overflow nor lose the argmax."""
+    n, d = 9, 16
+    for dtype in ("float16", "bfloat16"):
+        ks = np.zeros((n, 1, d), dtype=np.float32)
+        ks[:, 0, 0] = [-40, 0, 3, -40, 0, 40, 1, -40, 2]  # token 5 dominates
+        vs = np.arange(n * d, dtype=np.float32).reshape(n, 1, d) / 7.0
+        kc, vc, bt = build_pool([ks], [vs], [[2, 0, 1]], 4, 3, dtype)
+        qv = np.zeros((1, 1, d), dtype=np.float32)
+        qv[0, 0, 0] = 256.0  # score of token 5: 256 * 40 = 10240
+        out = oracle.attention(to_bits(qv, dtype), kc, vc, bt, [n], 1.0, dtype)
+        assert np.all(np.isfinite(out))
+        expect = widen(vc[bt[0, 5 // 4], 0, 5 % 4], dtype)  # token 5: block 0, slot 1
+        assert np.array_equal(out[0, 0], expect)
+        # negated query: the three keys of -40 tie at +10240 and share the weight
+        qv[0, 0, 0] = -256.0
+        out = oracle.attention(to_bits(qv, dtype), kc, vc, bt, [n], 1.0, dtype)
+        assert np.all(np.isfinite(out))
+        rows = [t for t in range(n) if ks[t, 0, 0] == -40]
+        mean = np.mean([widen(vc[bt[0, t // 4], 0, t % 4], dtype) for t in rows], axis=0)
+        assert len(rows) == 3 and np.allclose(out[0, 0], mean, rtol=1e-13, atol=1e-13)
+
+
+def pin_gqa_equals_replicated_mha():
+    rng = np.random.default_rng(4)
+    lengths = [7, 20, 1]
+    H_q, H_kv, d, B = 8, 2, 16, 4
+    q, kc, vc, bt, lens, _ = random_case(rng, lengths, H_q, H_kv, d, B, "bfloat16")
+    gqa = oracle.attention(q, kc, vc, bt, lens, 0.2, "bfloat16")
+    kc_rep = np.repeat(kc, H_q // H_kv, axis=1).copy()
+    vc_rep = np.repeat(vc, H_q // H_kv, axis=1).copy()
+    mha = oracle.attention(q, kc_rep, vc_rep, bt, lens, 0.2, "bfloat16")
+    assert np.array_equal(gqa, mha), "GQA must equal MHA over replicated KV heads"
+    # MQA: one KV head serves every query head
+    q1, kc1, vc1, bt1, lens1, _ = random_case(rng, lengths, 4, 1, d, B, "float16")
+    mqa = oracle.attention(q1, kc1, vc1, bt1, lens1, 0.2, "float16")
+    mha1 = oracle.attention(q1, np.repeat(kc1, 4, axis=1).copy(), np.repeat(vc1, 4, axis=1).copy(),
+                            bt1, lens1, 0.2, "float16")
+    assert np.array_equal(mqa, mha1)
+
+
+def pin_paging_invariance():
+    """Any physical placement of the same logical blocks gives the same output."""
+    rng = np.random.default_rng(5)
+    lengths = [13, 40, 4]
+    H, d, B = 2, 8, 4
+    ks = [rng.standard_normal((n, H, d)).astype(np.float32) for n in lengths]
+    vs = [rng.standard_normal((n, H, d)).astype(np.float32) for n in lengths]
+    need = [-(-n // B) for n in lengths]
+    nb = sum(need) + 2
+    q = to_bits(rng.standard_normal((3, H, d)), "float16")
+    outs = []
+    for trial in range(3):
+        perm = rng.permutation(nb)
+        tables, pos = [], 0
+        for k in need:
+            tables.append([int(b) for b in perm[pos:pos + k]])
+            pos += k
+        kc, vc, bt = build_pool(ks, vs, tables, B, nb, "float16", fill=float(trial))
+        outs.append(oracle.attention(q, kc, vc, bt, lengths, 0.35, "float16"))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def pin_shared_prefix_equals_private_copies():
+    rng = np.random.default_rng(6)
+    H, d, B = 1, 8, 4
+    prefix_k = rng.standard_normal((8, H, d)).astype(np.float32)
+    prefix_v = rng.standard_normal((8, H, d)).astype(np.float32)
+    tail_k = [rng.standard_normal((3, H, d)).astype(np.float32) for _ in range(2)]
+    tail_v = [rng.standard_normal((3, H, d)).astype(np.float32) for _ in range(2)]
+    ks = [np.concatenate([prefix_k, t]) for t in tail_k]
+    vs = [np.concatenate([prefix_v, t]) for t in tail_v]
+    q = to_bits(rng.standard_normal((2, H, d)), "bfloat16")
+    # private: every block its own
+    kc, vc, bt = build_pool(ks, vs, [[0, 1, 2], [3, 4, 5]], B, 6, "bfloat16")
+    private = oracle.attention(q, kc, vc, bt, [11, 11], 0.4, "bfloat16")
+    # shared: both sequences map their two prefix blocks onto blocks 4 and 1
+    kc2, vc2, bt2 = build_pool(ks, vs, [[4, 1, 0], [4, 1, 3]], B, 6, "bfloat16")
+    shared = oracle.attention(q, kc2, vc2, bt2, [11, 11], 0.4, "bfloat16")
+    assert np.array_equal(private, shared)
+
+
+def pin_online_recurrence_equals_two_pass():
+    """Eq. (4) over any chunking equals dense softmax (witness: 2.2e-16 scale)."""
+    with open(os.path.join(GOLDEN, "witness.json")) as f:
+        witness = json.load(f)
+    rng = np.random.default_rng(7)
+    lengths = [1, 16, 37, 91]
+    q, kc, vc, bt, lens, _ = random_case(rng, lengths, 4, 2, 32, 16, "bfloat16")
+    dense = oracle.attention(q, kc, vc, bt, lens, 1 / math.sqrt(32), "bfloat16")
+    worst = 0.0
+    cases = 0
+    for chunk in (1, 3, 7, 16, 64, 1000):
+        online = oracle.online_attention(q, kc, vc, bt, lens, 1 / math.sqrt(32), "bfloat16", chunk)
+        worst = max(worst, float(np.max(np.abs(online - dense))))
+        cases += 1
+    assert cases >= 1 and worst <= 64 * witness["largest_absolute_error"], worst
+
+
+def pin_partition_merge_equals_two_pass():
+    rng = np.random.default_rng(8)
+    lengths = [0, 5, 48, 100]
+    q, kc, vc, bt, lens, _ = random_case(rng, lengths, 4, 4, 16, 8, "float16")
+    dense = oracle.attention(q, kc, vc, bt, lens, 0.25, "float16")
+    for part in (8, 16, 40, 128):
+        parts = -(-max(lengths) // part)
+        m, l, acc = oracle.partition_stats(q, kc, vc, bt, lens, 0.25, "float16", part, parts)
+        merged = oracle.merge_partitions(m, l, acc)
+        assert np.max(np.abs(merged - dense)) <= 1e-14
+    # a single partition covering everything: l is the softmax denominator
+    m, l, acc = oracle.partition_stats(q, kc, vc, bt, lens, 0.25, "float16", 128, 1)
+    assert np.allclose(acc[:, :, 0, :] / np.where(l > 0, l, 1.0), dense, rtol=0, atol=1e-15)
+
+
+def pin_brute_force_against_library_softmax():
+    """Tiny random cases against scipy's softmax on explicitly gathered rows."""
+    rng = np.random.default_rng(9)
+    for dtype, B in (("float16", 2), ("bfloat16", 3)):
+        lengths = [1, 2, 5]
+        q, kc, vc, bt, lens, tables = random_case(rng, lengths, 2, 1, 4, B, dtype)
+        out = oracle.attention(q, kc, vc, bt, lens, 0.5, dtype)
+        for s, n in enumerate(lengths):
+            K = np.stack([widen(kc[tables[s][t // B], 0, t % B], dtype) for t in range(n)])
+            V = np.stack([widen(vc[tables[s][t // B], 0, t % B], dtype) for t in range(n)])
+            for i in range(2):
+                w = softmax(0.5 * (K @ widen(q[s, i], dtype)))
+                assert np.allclose(out[s, i], w @ V, rtol=1e-12, atol=1e-13)
+
+
+def pin_empty_sequence_is_zero():
+    rng = np.random.default_rng(10)
+    q, kc, vc, bt, lens, _ = random_case(rng, [0, 3], 2, 2, 8, 4, "bfloat16")
+    out = oracle.attention(q, kc, vc, bt, lens, 1.0, "bfloat16")
+    assert np.array_equal(out[0], np.zeros_like(out[0])) and np.any(out[1] != 0)
+
+
+# ---------------------------------------------------------------------------
+# kv_write and copy_blocks
+# ---------------------------------------------------------------------------
+def pin_kv_write_slot_arithmetic():
+    """slot = physical block * B + offset; negative slots are padding."""
+    H, d, B, nb = 2, 4, 4, 5
+    kc = np.zeros((nb, H, B, d), dtype=np.uint16)
+    vc = np.zeros_like(kc)
+    k = np.arange(3 * H * d, dtype=np.uint16).reshape(3, H, d) + 1
+    v = k + 1000
+    # token 0 -> block 1 slot 2 (slot 6); token 1 padding; token 2 -> block 4 slot 3 (slot 19)
+    kc2, vc2, status = oracle.kv_write(k, v, [6, -1, 19], kc, vc)
+    assert status == 0
+    assert np.array_equal(kc2[1, :, 2, :], k[0]) and np.array_equal(vc2[1, :, 2, :], v[0])
+    assert np.array_equal(kc2[4, :, 3, :], k[2]) and np.array_equal(vc2[4, :, 3, :], v[2])
+    changed = np.argwhere(kc2 != 0)
+    assert len(changed) == 2 * H * d  # nothing else touched, padding skipped
+    # a slot past the pool is reported and skipped
+    kc3, _, status = oracle.kv_write(k[:1], v[:1], [nb * B], kc, vc)
+    assert status != 0 and not kc3.any()
+
+
+def pin_kv_write_then_read_back():
+    """A token written at the next slot is the one a length-1 read returns."""
+    rng = np.random.default_rng(11)
+    H, d, B, nb = 2, 8, 4, 6
+    kc = to_bits(rng.standard_normal((nb, H, B, d)), "bfloat16")
+    vc = to_bits(rng.standard_normal((nb, H, B, d)), "bfloat16")
+    k = to_bits(rng.standard_normal((1, H, d)), "bfloat16")
+    v = to_bits(rng.standard_normal((1, H, d)), "bfloat16")
+    slot = 3 * B  # first slot of block 3
+    kc2, vc2, _ = oracle.kv_write(k, v, [slot], kc, vc)
+    q = to_bits(rng.standard_normal((1, H, d)), "bfloat16")
+    out = oracle.attention(q, kc2, vc2, np.array([[3]], dtype=np.int32), [1], 1.0, "bfloat16")
+    assert np.array_equal(out[0], widen(v[0], "bfloat16"))
+
+
+def pin_copy_blocks_copies_whole_blocks():
+    rng = np.random.default_rng(12)
+    H, d, B, nb = 2, 4, 4, 6
+    kc = rng.integers(0, 65535, (nb, H, B, d), dtype=np.uint16)
+    vc = rng.integers(0, 65535, (nb, H, B, d), dtype=np.uint16)
+    kc2, vc2, status = oracle.copy_blocks(kc, vc, [(1, 4), (2, 0)])
+    assert status == 0
+    assert np.array_equal(kc2[4], kc[1]) and np.array_equal(vc2[4], vc[1])
+    assert np.array_equal(kc2[0], kc[2]) and np.array_equal(vc2[0], vc[2])
+    for b in (1, 2, 3, 5):
+        assert np.array_equal(kc2[b], kc[b]) and np.array_equal(vc2[b], vc[b])
+    _, _, status = oracle.copy_blocks(kc, vc, [(1, nb)])
+    assert status != 0
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

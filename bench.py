@@ -1,0 +1,465 @@
+"""Decode-step benchmark: paged decode attention HBM GB/s and decode tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+Workload (one step = the whole hot path over one batch): the GQA decode
+batch -- 64 sequences with context lengths uniform on 512..4096, block size
+16, 32 query heads over 8 KV heads, head dim 128, bf16, blocks shuffled over
+a pool of 1.2x the blocks needed.  Each step writes one new token per
+sequence into its slot (kv_write, preceded by copy_blocks when the block
+manager reports copy-on-write pairs: none for this batch) and runs paged
+decode attention over context + 1 tokens (split into 512-token partitions
+with the log-sum-exp merge).  The KV pools (~0.7 GB) are larger than L2, so
+no flush is needed between steps.
+
+``value`` is algorithmic bytes per step (K + V of every attended token, q,
+out, the block-table entries and sequence lengths read, and kv_write's
+reads and writes) over the device time of a step.  ``roofline`` reports the
+paged_decode_attention call alone against the measured HBM peak.
+
+With N > 1 (torchrun), every rank runs its own replica of the batch (weak
+scaling, no collective on the data path); the time is the max over ranks.
+
+``--impl reference`` times the CPU oracle (fp64, OpenMP) on a bounded sample
+of the same batch and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "paged decode attention achieved HBM GB/s (% of GB300 peak) and decode tokens/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-extra", action="store_true", help="skip the long-context line")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=244)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# accounting
+# ----------------------------------------------------------------------------
+def attention_bytes(step) -> int:
+    """Algorithmic bytes of one paged_decode_attention call."""
+    lens = step.seq_lens.to(torch.int64)
+    b = 2  # bytes per scalar
+    kv = int(lens.sum()) * step.num_kv_heads * step.head_dim * b * 2
+    qo = 2 * step.num_seqs * step.num_q_heads * step.head_dim * b
+    tables = int(((lens + step.block_size - 1) // step.block_size).sum()) * 4 + 4 * step.num_seqs
+    return kv + qo + tables
+
+
+def kv_write_bytes(step) -> int:
+    T = int(step.slot_mapping.numel())
+    return 2 * (2 * T * step.num_kv_heads * step.head_dim * 2) + 8 * T
+
+
+def copy_bytes(step) -> int:
+    per_block = step.num_kv_heads * step.block_size * step.head_dim * 2 * 2  # K and V
+    return int(step.cow_pairs.shape[0]) * per_block * 2  # read + write
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_for(source: str):
+    """DRAM bytes per launch from a committed ncu capture of this exact source."""
+    path = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    digest = hashlib.sha256(open(source, "rb").read()).hexdigest()
+    if rec.get("source_sha256") != digest:
+        return None
+    return rec.get("dram_bytes_per_launch_gqa_batch")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample_rate(step, max_seconds: float, max_seqs=None, min_reps=1):
+    """Run the oracle (kv_write replay + attention) on the first sequences.
+
+    Returns (bytes per second, seconds, description, threads).
+    """
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_242_gb300.workloads import bits
+
+    S = step.num_seqs if max_seqs is None else min(max_seqs, step.num_seqs)
+    threads = oracle.max_threads()
+    kc, vc = bits(step.k_cache), bits(step.v_cache)
+    q = np.ascontiguousarray(bits(step.q)[:S])
+    bt = np.ascontiguousarray(step.block_tables.numpy()[:S])
+    sl = np.ascontiguousarray(step.seq_lens.numpy()[:S])
+    kn = np.ascontiguousarray(bits(step.k_new)[:S])
+    vn = np.ascontiguousarray(bits(step.v_new)[:S])
+    slots = np.ascontiguousarray(step.slot_mapping.numpy()[:S])
+    per_rep = (int(sl.astype(np.int64).sum()) * step.num_kv_heads * step.head_dim * 4 +
+               2 * S * step.num_q_heads * step.head_dim * 2)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        kc2, vc2, _ = oracle.kv_write(kn, vn, slots, kc, vc)
+        oracle.attention(q, kc2, vc2, bt, sl, step.scale, step.dtype, num_threads=threads)
+        reps += 1
+        elapsed = time.perf_counter() - t0
+        if reps >= min_reps and elapsed >= max_seconds:
+            break
+    desc = (f"{S} of {step.num_seqs} sequences of the batch (kv_write replay + fp64 attention), "
+            f"{reps} repetition(s), {elapsed:.1f} s")
+    return per_rep * reps / elapsed, elapsed / reps, desc, threads
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, timed on the host, on rank 0 only."""
+    if rank != 0:
+        return
+    from paged_kv_cache_242_gb300 import workloads as W
+
+    step = W.gqa_batch(seed=args.seed)
+    # size the per-step sample so K + W steps end within ~2 minutes
+    probe_rate, probe_t, _, _ = oracle_sample_rate(step, 0.0, max_seqs=1)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    seqs = max(1, min(step.num_seqs, int(budget / max(probe_t, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample_rate(step, 0.0, max_seqs=seqs)
+    t0 = time.perf_counter()
+    per_bytes = 0.0
+    for _ in range(args.steps):
+        rate, t_rep, desc, threads = oracle_sample_rate(step, 0.0, max_seqs=seqs)
+        per_bytes += rate * t_rep
+    elapsed = time.perf_counter() - t0
+    value = per_bytes / elapsed / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * elapsed / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(step),
+        "cpu_baseline": {"kind": "oracle", "value": round(value, 4), "unit": UNIT,
+                         "cores": threads, "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(step, partition=None):
+    cfg = {"workload": "gqa_decode_batch", "num_seqs": step.num_seqs,
+           "context_lengths": "uniform 512..4096 (+1 written token)",
+           "num_q_heads": step.num_q_heads, "num_kv_heads": step.num_kv_heads,
+           "head_dim": step.head_dim, "block_size": step.block_size,
+           "num_blocks": int(step.k_cache.shape[0]) if step.k_cache is not None else None,
+           "kv_tokens": step.kv_tokens, "max_seq_len": step.max_seq_len,
+           "l2": "inputs larger than L2 (no flush)"}
+    if partition is not None:
+        cfg["partition_size"] = partition
+    return cfg
+
+
+def time_attention_only(pkv, step, dev, part, reps=200, warmup=10):
+    """Average device time of one paged_decode_attention call (CUDA events)."""
+    ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
+                                          step.block_size, part)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev["q"].device)
+    out = torch.empty_like(dev["q"])
+
+    def call():
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["seq_lens"], step.num_kv_heads, step.scale, out,
+                                   max_seq_len=step.max_seq_len, partition_size=part,
+                                   workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_pkv(args, rank, world, local_rank):
+    import paged_kv_cache_242_gb300 as pkv
+    from paged_kv_cache_242_gb300 import workloads as W
+
+    pkv._lib.load()  # fail loudly: no fallback
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    step = W.gqa_batch(seed=args.seed + 7919 * rank)
+    dev = {k: v.to(device) for k, v in {
+        "q": step.q, "k_new": step.k_new, "v_new": step.v_new, "slot_mapping": step.slot_mapping,
+        "block_tables": step.block_tables, "seq_lens": step.seq_lens,
+        "cow_pairs": step.cow_pairs, "k_cache": step.k_cache, "v_cache": step.v_cache}.items()}
+    part = pkv.decode_partition_size(step.max_seq_len, step.block_size, args.partition_size)
+    split = part < step.max_seq_len
+    ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
+                                          step.block_size, args.partition_size)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    out = torch.empty_like(dev["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    has_cow = step.cow_pairs.numel() > 0
+
+    def attention():
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["seq_lens"], step.num_kv_heads, step.scale, out,
+                                   max_seq_len=step.max_seq_len,
+                                   partition_size=args.partition_size, workspace=workspace,
+                                   err_flag=err)
+
+    def write():
+        if has_cow:
+            pkv.copy_blocks(dev["k_cache"], dev["v_cache"], dev["cow_pairs"], err_flag=err)
+        pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                     dev["v_cache"], err_flag=err)
+
+    launches_per_step = 1 + (1 if has_cow else 0) + 1 + (1 if split else 0)
+    for _ in range(max(3, args.warmup)):
+        write()
+        attention()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        write()
+        ev[i][0].record(stream)
+        attention()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(end)
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    a_bytes = attention_bytes(step)
+    step_bytes = a_bytes + kv_write_bytes(step) + copy_bytes(step)
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    tokens_per_s = world * step.num_seqs / (ms_per_step * 1e-3)
+
+    # ---------------- end to end through the public API ----------------
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in {
+            "q": step.q, "k_new": step.k_new, "v_new": step.v_new,
+            "slot_mapping": step.slot_mapping, "block_tables": step.block_tables,
+            "seq_lens": step.seq_lens}.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = out_host.numel() * out_host.element_size()
+        inputs = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
+        e2e_steps = max(10, min(K, 2000))
+
+        def e2e_step():
+            for k in pin:
+                inputs[k].copy_(pin[k], non_blocking=True)
+            pkv.kv_write(inputs["k_new"], inputs["v_new"], inputs["slot_mapping"],
+                         dev["k_cache"], dev["v_cache"], err_flag=err)
+            pkv.paged_decode_attention(inputs["q"], dev["k_cache"], dev["v_cache"],
+                                       inputs["block_tables"], inputs["seq_lens"],
+                                       step.num_kv_heads, step.scale, out,
+                                       max_seq_len=step.max_seq_len,
+                                       partition_size=args.partition_size, workspace=workspace,
+                                       err_flag=err)
+            out_host.copy_(out, non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": round(world * (a_bytes + kv_write_bytes(step)) / e2e_s / 1e9, 2),
+               "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3, 4), "steps": e2e_steps,
+               "decode_tokens_per_s": round(world * step.num_seqs / e2e_s, 1)}
+
+    # ---------------- long-context batch: attention alone ----------------
+    extra = {}
+    if not args.no_extra and rank == 0:
+        del dev, workspace
+        torch.cuda.empty_cache()
+        lc = W.long_context()
+        dlc = {"q": lc.q.to(device), "k_cache": lc.k_cache.to(device),
+               "v_cache": lc.v_cache.to(device), "block_tables": lc.block_tables.to(device),
+               "seq_lens": lc.seq_lens.to(device)}
+        lc_ms = time_attention_only(pkv, lc, dlc, 0)
+        hbm, kind = measured_peaks()
+        lc_gbs = attention_bytes(lc) / (lc_ms * 1e-3) / 1e9
+        extra["long_context"] = {
+            "workload": "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16, "
+                        "512-token partitions + merge",
+            "attention_ms": round(lc_ms, 4), "achieved_gbs": round(lc_gbs, 1),
+            "frac_of_measured_peak": round(lc_gbs / hbm, 4),
+            "frac_of_nominal_8tbs": round(lc_gbs / NOMINAL_HBM_GBS, 4),
+            "decode_tokens_per_s": round(lc.num_seqs / (lc_ms * 1e-3), 1)}
+        del dlc
+
+    if rank != 0:
+        return
+    hbm, kind = measured_peaks()
+    achieved = a_bytes / (attn_ms * 1e-3) / 1e9
+    source = os.path.join(ROOT, "paged_kv_cache_242_gb300", "csrc", "decode_attention.cu")
+    roofline = {"kernel": "paged_decode_attention (partition kernel + merge kernel)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "peak_kind": f"{kind} (burst copy)",
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                "algorithmic_bytes_per_launch": a_bytes,
+                "avg_call_ms": round(attn_ms, 5),
+                "traffic": traffic_for(source)}
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        rate, _, desc, threads = oracle_sample_rate(step, 10.0)
+        cpu = {"kind": "oracle", "value": round(rate / 1e9, 4), "unit": UNIT, "cores": threads,
+               "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(step, part),
+        "decode_tokens_per_s": round(tokens_per_s, 1),
+        "step_bytes": step_bytes, "gpu_launches": launches_per_step * K,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clock_info,
+    }
+    if extra:
+        line["extra"] = extra
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_pkv(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

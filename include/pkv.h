@@ -1,0 +1,198 @@
+/*
+ * pkv.h — C ABI of libpkv.so: paged KV-cache decode path on one GPU.
+ *
+ * Three operations, each a hand-written CUDA kernel for sm_103a:
+ *   pkv_kv_write                write new keys / values into cache slots
+ *   pkv_paged_decode_attention  one-query-token attention over paged K/V
+ *   pkv_copy_blocks             whole-block copies for copy-on-write
+ *
+ * Storage.  The key cache and the value cache are two separate pools of
+ * fixed-size physical blocks, each laid out row-major as
+ *     [num_blocks][num_kv_heads][block_size][head_dim]
+ * so one (block, KV head) tile of block_size x head_dim scalars is contiguous
+ * (at block size 16 and head size 128 that is 2048 elements per head per
+ * block).  Scalars are IEEE binary16 or bfloat16.  A sequence reaches its
+ * tokens through a block table: logical token t of sequence s lives in
+ * physical block block_tables[s][t / block_size], slot t % block_size.
+ * (vLLM PagedAttention & continuous batching, "PagedAttention: fixed blocks,
+ * non-contiguous physical memory" and "The kernel page".)
+ *
+ * Conventions common to every call.
+ *  - Every pointer argument except those documented as host values is a
+ *    DEVICE pointer.  The caller owns every buffer; the library allocates
+ *    nothing and keeps no state between calls.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is enqueued asynchronously on it.
+ *  - Arguments are validated on the host before anything is enqueued; on a
+ *    validation failure the call returns PKV_ERR_INVALID_ARG or
+ *    PKV_ERR_UNSUPPORTED and enqueues nothing.  A failed launch returns
+ *    PKV_ERR_CUDA.
+ *  - Errors that depend on device data (a block id outside the pool, a slot
+ *    outside the pool, a sequence longer than its block table, a bad block
+ *    pair) never trap: the kernel skips the offending access and ORs one of
+ *    the PKV_DEVERR_* bits into *err_flag when err_flag is not NULL.  The
+ *    caller reads the flag after synchronising the stream.
+ *  - Calls on the same stream execute in order; calls that touch the same
+ *    cache from different streams must be ordered by the caller.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,          /* null pointer, negative size, inconsistent shapes */
+    PKV_ERR_UNSUPPORTED = 2,          /* a valid shape this build does not implement */
+    PKV_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace smaller than pkv_decode_workspace_bytes */
+    PKV_ERR_CUDA = 4                  /* a CUDA launch or driver call failed */
+} pkv_status;
+
+typedef enum { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits ORed into *err_flag by the kernels (device-side data errors). */
+#define PKV_DEVERR_BAD_SLOT     1  /* slot_mapping[t] >= num_blocks * block_size */
+#define PKV_DEVERR_BAD_BLOCK_ID 2  /* a block-table entry outside [0, num_blocks) */
+#define PKV_DEVERR_BAD_SEQ_LEN  4  /* seq_len < 0, > max_seq_len or > table capacity */
+#define PKV_DEVERR_BAD_PAIR     8  /* a copy pair with src or dst outside [0, num_blocks) */
+#define PKV_DEVERR_TIMEOUT      16 /* a bounded on-chip wait gave up (never expected) */
+
+/* Geometry of both caches (host value). */
+typedef struct {
+    int32_t num_blocks;    /* physical blocks in each pool, > 0 */
+    int32_t num_kv_heads;  /* KV heads, > 0 */
+    int32_t block_size;    /* token slots per block */
+    int32_t head_dim;      /* scalars per head */
+    pkv_dtype dtype;       /* storage type of caches, q, k, v and out */
+} pkv_cache_desc;
+
+/*
+ * Write the keys and values of new tokens into their cache slots.
+ *
+ * Decode writes the next token of a sequence into the spare slot of its last
+ * block (vLLM PagedAttention & continuous batching, "PagedAttention", the
+ * seven-token example); prefill writes every prompt token the same way.
+ * The slot of token t is slot_mapping[t] = physical_block * block_size +
+ * offset, so for every KV head h:
+ *     k_cache[slot / B][h][slot % B][:] = k[t][h][:]   (and v likewise).
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim], dtype of c, contiguous.
+ *   slot_mapping  [num_tokens] int64.  A negative slot marks a padding token
+ *                 and is skipped silently; a slot >= num_blocks * block_size
+ *                 is skipped and sets PKV_DEVERR_BAD_SLOT.
+ *   k_cache, v_cache  the pools, updated in place.
+ *   Slots must be distinct among non-negative entries (two tokens written to
+ *   one slot race).  head_dim must be a multiple of 8 and every row 16-byte
+ *   aligned.  num_tokens == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                        int32_t num_tokens, void* k_cache, void* v_cache, pkv_cache_desc c,
+                        int32_t* err_flag, void* stream);
+
+/*
+ * Partition size (tokens) that pkv_paged_decode_attention uses for the
+ * given request: `partition_size` itself when positive (it must then be a
+ * multiple of block_size), else the automatic choice (512 tokens when
+ * max_seq_len > 512, otherwise a single partition).  Returns a value
+ * >= max_seq_len when every sequence is handled in one pass, or -1 when the
+ * arguments are invalid.
+ */
+PKV_API int32_t pkv_decode_partition_size(int32_t max_seq_len, int32_t block_size,
+                                  int32_t partition_size);
+
+/*
+ * Workspace bytes pkv_paged_decode_attention needs for these sizes (0 when
+ * every sequence fits one partition).  The workspace holds per-partition
+ * fp32 statistics: an accumulator row of head_dim floats plus a running
+ * maximum and a running sum for each (sequence, query head, partition).
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                  int32_t max_seq_len, int32_t block_size,
+                                  int32_t partition_size);
+
+/*
+ * Exact attention of one query token per sequence over its paged K/V.
+ *
+ * For sequence s, query head i and its KV head h = i / (num_q_heads /
+ * num_kv_heads) (contiguous grouped-query groups; MHA when the ratio is 1,
+ * MQA when num_kv_heads is 1):
+ *     out[s][i] = sum_t softmax_t(scale * q[s][i] . K_t) V_t,  t < seq_lens[s],
+ * with K_t, V_t read through block_tables[s].  PagedAttention leaves this
+ * formula unchanged and only changes where K and V live (vLLM PagedAttention
+ * & continuous batching, "PagedAttention" and "The kernel page").  The
+ * softmax is computed block by block with the running maximum / running sum
+ * of Eq. (4) of "Serving Language Models Within a Memory Budget"; sequences
+ * longer than one partition are split into partitions whose (max, sum,
+ * weighted-sum) statistics are merged by the same rule.  Products of
+ * fp16/bf16 inputs accumulate in fp32; the output is rounded to the storage
+ * dtype (round to nearest even).  An empty sequence (seq_len 0) yields zeros.
+ *
+ *   q             [num_seqs][num_q_heads][head_dim], contiguous.
+ *   k_cache, v_cache  pools (see top); 16-byte aligned.
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32; only the first
+ *                 ceil(seq_len / block_size) entries of a row are read.
+ *   seq_lens      [num_seqs] int32 attended lengths.
+ *   max_seq_len   HOST value, an upper bound of every seq_lens[s]; it sizes
+ *                 the launch without a device-to-host read.  Must be
+ *                 <= max_blocks_per_seq * block_size.
+ *   scale         softmax scale, typically 1/sqrt(head_dim).
+ *   partition_size  0 = automatic; > 0 tokens per partition (a multiple of
+ *                 block_size); >= max_seq_len = single pass.
+ *   workspace     device scratch of workspace_bytes >=
+ *                 pkv_decode_workspace_bytes(...) (may be NULL when that is 0).
+ *                 Its contents need no initialisation and are overwritten.
+ *   out           [num_seqs][num_q_heads][head_dim], dtype of c.
+ * Supported: head_dim 128, block_size 16 or 32, num_q_heads / num_kv_heads
+ * <= 64, num_seqs <= 65535; other valid shapes return PKV_ERR_UNSUPPORTED.
+ */
+PKV_API pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t max_seq_len,
+                                      int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c,
+                                      float scale, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, void* out, int32_t* err_flag,
+                                      void* stream);
+
+/*
+ * Copy whole physical blocks, for copy-on-write of a shared block.
+ *
+ * When a sequence must write into a block whose reference count is above
+ * one, the block manager allocates a fresh block and the old block's
+ * contents are copied into it (vLLM PagedAttention & continuous batching,
+ * "Sharing with reference counts and copy-on-write"; the last partial block
+ * of a shared prefix is copy-on-write).  For each pair p:
+ *     k_cache[dst_p] = k_cache[src_p],  v_cache[dst_p] = v_cache[src_p]
+ * over every KV head and every slot, filled or not, bit for bit.
+ *
+ *   src_dst_pairs  DEVICE [num_pairs][2] int64 (src, dst).  Destinations
+ *                  must be distinct and no destination may be the source of
+ *                  another pair (pairs run concurrently).  A pair with an
+ *                  index outside [0, num_blocks) is skipped and sets
+ *                  PKV_DEVERR_BAD_PAIR.  num_pairs == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc c,
+                           const int64_t* src_dst_pairs, int32_t num_pairs, int32_t* err_flag,
+                           void* stream);
+
+/* Static, NUL-terminated name of a status code. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* ABI version of this header (major * 100 + minor). */
+PKV_API int32_t pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

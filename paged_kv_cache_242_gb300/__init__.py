@@ -1,0 +1,22 @@
+"""GB300-native paged KV-cache decode path.
+
+The KV cache lives in fixed-size, non-contiguous physical blocks reached
+through per-sequence block tables.  Three hand-written sm_103a CUDA kernels,
+behind the C ABI of ``libpkv.so`` (``include/pkv.h``), do the work:
+
+* ``kv_write``               scatter new keys / values into block slots;
+* ``paged_decode_attention`` exact one-query-token attention over the blocks
+                             (MHA, GQA, MQA; split over long sequences with a
+                             log-sum-exp merge);
+* ``copy_blocks``            whole-block copies for copy-on-write.
+
+``block_manager`` is the host-side block table / refcount manager that
+produces the kernels' inputs; ``workloads`` generates seeded synthetic
+decode batches.
+"""
+from ._lib import PKVError  # noqa: F401
+from .ops import (cache_desc, copy_blocks, decode_partition_size,  # noqa: F401
+                  decode_workspace_bytes, kv_write, paged_decode_attention)
+
+__all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
+           "decode_partition_size", "cache_desc", "PKVError"]

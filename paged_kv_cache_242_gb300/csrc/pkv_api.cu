@@ -1,0 +1,223 @@
+// The C ABI of libpkv.so (declared in include/pkv.h): host-side argument
+// validation, TMA descriptor encoding and kernel dispatch.  Nothing here
+// allocates device memory or keeps state beyond a cached driver entry point.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pkv_internal.h"
+
+namespace {
+
+using pkv::kAutoPartition;
+using pkv::kHeadDim;
+
+bool aligned(const void* p, uintptr_t bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+
+bool valid_dtype(pkv_dtype d) { return d == PKV_FP16 || d == PKV_BF16; }
+
+// Geometry checks shared by every call.
+pkv_status check_cache(const pkv_cache_desc& c) {
+    if (c.num_blocks <= 0 || c.num_kv_heads <= 0 || c.block_size <= 0 || c.head_dim <= 0 ||
+        !valid_dtype(c.dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (c.head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;  // 16-byte rows
+    return PKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A 4-D view of one pool, {head_dim, block_size, num_kv_heads, num_blocks}
+// (innermost first), tiled in boxes of {64, block_size, 1, 1} with the
+// 128-byte swizzle: one box is one half (64 columns) of a (block, head) tile.
+bool encode_pool(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t row = static_cast<cuuint64_t>(c.head_dim) * 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.head_dim), static_cast<cuuint64_t>(c.block_size),
+                          static_cast<cuuint64_t>(c.num_kv_heads),
+                          static_cast<cuuint64_t>(c.num_blocks)};
+    cuuint64_t strides[3] = {row, row * c.block_size, row * c.block_size * c.num_kv_heads};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(c.block_size), 1, 1};
+    cuuint32_t elem[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType type =
+        c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = encode(map, type, 4, const_cast<void*>(base), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Effective partition size: >= max_seq_len means one pass per sequence.
+int32_t effective_partition(int32_t max_seq_len, int32_t block_size, int32_t partition_size) {
+    if (max_seq_len < 0 || block_size <= 0 || partition_size < 0) return -1;
+    const int64_t single = round_up(max_seq_len > 0 ? max_seq_len : 1, block_size);
+    int64_t part;
+    if (partition_size == 0) {
+        part = max_seq_len > kAutoPartition ? kAutoPartition : single;
+        if (part % block_size != 0) part = round_up(part, block_size);
+    } else {
+        if (partition_size % block_size != 0) return -1;
+        part = partition_size;
+    }
+    if (part >= single) part = single;
+    return static_cast<int32_t>(part);
+}
+
+int32_t partitions_for(int32_t max_seq_len, int32_t part) {
+    const int32_t n = max_seq_len > 0 ? max_seq_len : 1;
+    return static_cast<int32_t>((static_cast<int64_t>(n) + part - 1) / part);
+}
+
+size_t workspace_for(int32_t num_seqs, int32_t num_q_heads, int32_t max_partitions) {
+    if (max_partitions <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_partitions;
+    return rows * (kHeadDim + 2) * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkv_abi_version(void) { return 100; }
+
+const char* pkv_status_string(pkv_status status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    }
+    return "PKV_UNKNOWN_STATUS";
+}
+
+pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                        int32_t num_tokens, void* k_cache, void* v_cache, pkv_cache_desc c,
+                        int32_t* err_flag, void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::launch_kv_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, c,
+                                         err_flag, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int32_t pkv_decode_partition_size(int32_t max_seq_len, int32_t block_size, int32_t partition_size) {
+    return effective_partition(max_seq_len, block_size, partition_size);
+}
+
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                  int32_t max_seq_len, int32_t block_size,
+                                  int32_t partition_size) {
+    (void)head_dim;
+    if (num_seqs <= 0 || num_q_heads <= 0) return 0;
+    const int32_t part = effective_partition(max_seq_len, block_size, partition_size);
+    if (part <= 0) return 0;
+    return workspace_for(num_seqs, num_q_heads, partitions_for(max_seq_len, part));
+}
+
+pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t max_seq_len,
+                                      int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c,
+                                      float scale, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, void* out, int32_t* err_flag,
+                                      void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+        partition_size < 0 || !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % c.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * c.block_size)
+        return PKV_ERR_INVALID_ARG;
+    if (partition_size > 0 && partition_size % c.block_size != 0) return PKV_ERR_INVALID_ARG;
+    if (c.head_dim != kHeadDim || (c.block_size != 16 && c.block_size != 32) ||
+        num_q_heads / c.num_kv_heads > 64 || num_seqs > 65535 || c.num_kv_heads > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+
+    const int32_t part = effective_partition(max_seq_len, c.block_size, partition_size);
+    const int32_t max_parts = partitions_for(max_seq_len, part);
+    const size_t need = workspace_for(num_seqs, num_q_heads, max_parts);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && !aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+
+    CUtensorMap k_map, v_map;
+    if (!encode_pool(&k_map, k_cache, c) || !encode_pool(&v_map, v_cache, c)) return PKV_ERR_CUDA;
+
+    pkv::DecodeArgs a{};
+    a.q = q;
+    a.out = out;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    if (need > 0) {
+        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+        float* ws = static_cast<float*>(workspace);
+        a.ws_acc = ws;
+        a.ws_m = ws + rows * kHeadDim;
+        a.ws_l = a.ws_m + rows;
+    }
+    a.err = err_flag;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = c.num_kv_heads;
+    a.group = num_q_heads / c.num_kv_heads;
+    a.num_blocks = c.num_blocks;
+    a.partition_size = part;
+    a.max_partitions = max_parts;
+    a.max_seq_len = max_seq_len;
+    a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    cudaError_t e =
+        pkv::launch_paged_decode(k_map, v_map, a, c.dtype, c.block_size, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc c,
+                           const int64_t* src_dst_pairs, int32_t num_pairs, int32_t* err_flag,
+                           void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src_dst_pairs) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst_pairs, 8))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
+    if ((vecs + 1023) / 1024 > 65535) return PKV_ERR_UNSUPPORTED;
+    cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, c, src_dst_pairs, num_pairs,
+                                            err_flag, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+"""Python binding of the three kernels: argument marshalling only.
+
+Every function takes torch CUDA tensors, checks their shapes / dtypes /
+layout, and calls the matching ``pkv_*`` entry point of libpkv.so with raw
+device pointers and the current CUDA stream.  All arithmetic runs in the
+library's CUDA kernels; if the library is missing the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import CacheDesc, PKVError
+
+_DTYPES = {torch.float16: _lib.PKV_FP16, torch.bfloat16: _lib.PKV_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    _require(k_cache.dim() == 4, "caches must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    _require(k_cache.dtype in _DTYPES, f"unsupported cache dtype {k_cache.dtype}")
+    nb, hkv, bs, d = k_cache.shape
+    return CacheDesc(int(nb), int(hkv), int(bs), int(d), _DTYPES[k_cache.dtype])
+
+
+def _check_caches(k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    _require(k_cache.is_cuda and v_cache.is_cuda, "caches must be CUDA tensors")
+    _require(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype,
+             "k_cache and v_cache must match in shape and dtype")
+    _require(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+
+
+def _err_ptr(err_flag: Optional[torch.Tensor]) -> Optional[int]:
+    if err_flag is None:
+        return None
+    _require(err_flag.dtype == torch.int32 and err_flag.is_cuda and err_flag.numel() >= 1,
+             "err_flag must be a CUDA int32 tensor")
+    return err_flag.data_ptr()
+
+
+def kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor,
+             err_flag: Optional[torch.Tensor] = None) -> None:
+    """Write k, v [T, H_kv, d] into the caches at ``slot_mapping`` (int64 [T])."""
+    _check_caches(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    T = int(slot_mapping.numel())
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and
+             slot_mapping.is_contiguous(), "slot_mapping must be a contiguous CUDA int64 tensor")
+    _require(k.shape == (T, desc.num_kv_heads, desc.head_dim) and v.shape == k.shape,
+             "k and v must be [num_tokens, num_kv_heads, head_dim]")
+    _require(k.dtype == k_cache.dtype and v.dtype == k_cache.dtype, "k/v dtype must match the cache")
+    _require(k.is_contiguous() and v.is_contiguous() and k.is_cuda and v.is_cuda,
+             "k and v must be contiguous CUDA tensors")
+    lib = _lib.load()
+    _lib.check(lib.pkv_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache),
+                                _ptr(v_cache), desc, _err_ptr(err_flag), _stream(k_cache.device)),
+               "pkv_kv_write")
+
+
+def decode_partition_size(max_seq_len: int, block_size: int, partition_size: int = 0) -> int:
+    return int(_lib.load().pkv_decode_partition_size(int(max_seq_len), int(block_size),
+                                                      int(partition_size)))
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, max_seq_len: int, block_size: int,
+                           partition_size: int = 0, head_dim: int = 128) -> int:
+    return int(_lib.load().pkv_decode_workspace_bytes(int(num_seqs), int(num_q_heads),
+                                                       int(head_dim), int(max_seq_len),
+                                                       int(block_size), int(partition_size)))
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                           num_kv_heads: Optional[int] = None, scale: Optional[float] = None,
+                           out: Optional[torch.Tensor] = None, *,
+                           max_seq_len: Optional[int] = None, partition_size: int = 0,
+                           workspace: Optional[torch.Tensor] = None,
+                           err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Attention of one query token per sequence over its paged K/V.
+
+    q [S, H_q, d]; block_tables int32 [S, max_blocks]; seq_lens int32 [S].
+    ``max_seq_len`` (a host int >= every seq_len) avoids a device read; if
+    omitted it is taken from ``seq_lens`` with a synchronising ``.item()``.
+    ``workspace`` (uint8 CUDA tensor) is allocated when needed and omitted.
+    """
+    _check_caches(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    if num_kv_heads is not None:
+        _require(int(num_kv_heads) == desc.num_kv_heads, "num_kv_heads disagrees with the cache")
+    _require(q.dim() == 3 and q.shape[2] == desc.head_dim, "q must be [num_seqs, num_q_heads, d]")
+    _require(q.dtype == k_cache.dtype and q.is_cuda and q.is_contiguous(),
+             "q must be a contiguous CUDA tensor of the cache dtype")
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+             block_tables.shape[0] == S and block_tables.is_contiguous() and block_tables.is_cuda,
+             "block_tables must be a contiguous CUDA int32 [num_seqs, max_blocks] tensor")
+    _require(seq_lens.dtype == torch.int32 and seq_lens.numel() == S and seq_lens.is_cuda and
+             seq_lens.is_contiguous(), "seq_lens must be a contiguous CUDA int32 [num_seqs] tensor")
+    if scale is None:
+        scale = desc.head_dim ** -0.5
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if S > 0 else 0
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous() and out.is_cuda,
+             "out must match q")
+    max_blocks = int(block_tables.shape[1])
+    need = decode_workspace_bytes(S, Hq, max_seq_len, desc.block_size, partition_size,
+                                  desc.head_dim)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    _lib.check(lib.pkv_paged_decode_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(seq_lens),
+        int(max_seq_len), S, Hq, desc, ctypes.c_float(float(scale)), int(partition_size),
+        _ptr(workspace), ws_bytes, _ptr(out), _err_ptr(err_flag), _stream(q.device)),
+        "pkv_paged_decode_attention")
+    return out
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor,
+                err_flag: Optional[torch.Tensor] = None) -> None:
+    """Copy whole blocks src -> dst of both caches; pairs int64 [P, 2] on the device."""
+    _check_caches(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.is_cuda and
+             src_dst_pairs.is_contiguous() and (src_dst_pairs.numel() == 0 or
+                                                src_dst_pairs.shape[-1] == 2),
+             "src_dst_pairs must be a contiguous CUDA int64 [num_pairs, 2] tensor")
+    P = int(src_dst_pairs.numel() // 2)
+    lib = _lib.load()
+    _lib.check(lib.pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), desc, _ptr(src_dst_pairs), P,
+                                   _err_ptr(err_flag), _stream(k_cache.device)),
+               "pkv_copy_blocks")
+
+
+__all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
+           "decode_partition_size", "cache_desc", "PKVError"]

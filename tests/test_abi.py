@@ -1,0 +1,116 @@
+"""The C ABI library loads and exports every symbol include/pkv.h declares.
+
+No compute runs here: only host-side queries and argument validation, which
+return before any CUDA call.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_cache_242_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for expected in ("pkv_kv_write", "pkv_paged_decode_attention", "pkv_copy_blocks",
+                     "pkv_decode_workspace_bytes", "pkv_status_string"):
+        assert expected in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    exported = subprocess.run(["nm", "-D", "--defined-only", build.LIBRARY], capture_output=True,
+                              text=True, check=True).stdout
+    symbols = {line.split()[-1] for line in exported.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in symbols, f"{name} declared in pkv.h but not exported"
+        assert hasattr(lib, name)
+    # nothing but the pkv_ API leaks out of the library
+    assert all(s.startswith("pkv_") for s in symbols), sorted(s for s in symbols if not s.startswith("pkv_"))
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE_TOO_SMALL"
+    assert lib.pkv_abi_version() == 100
+
+
+def test_partition_and_workspace_queries(lib):
+    assert lib.pkv_decode_partition_size(4097, 16, 0) == 512
+    assert lib.pkv_decode_partition_size(300, 16, 0) == 304  # single pass, rounded to blocks
+    assert lib.pkv_decode_partition_size(300, 16, 64) == 64
+    assert lib.pkv_decode_partition_size(300, 16, 24) == -1  # not a multiple of the block size
+    assert lib.pkv_decode_partition_size(32768, 16, 1 << 20) == 32768
+    # 64 seqs x 32 heads x ceil(4097/512)=9 partitions x (128 + 2) floats
+    assert lib.pkv_decode_workspace_bytes(64, 32, 128, 4097, 16, 0) == 64 * 32 * 9 * 130 * 4
+    assert lib.pkv_decode_workspace_bytes(5, 8, 128, 511, 16, 0) == 0
+
+
+def _desc(**kw):
+    d = dict(num_blocks=64, num_kv_heads=8, block_size=16, head_dim=128, dtype=1)
+    d.update(kw)
+    return _lib.CacheDesc(**d)
+
+
+def test_host_validation_without_launch(lib):
+    """Invalid arguments are rejected before any CUDA call."""
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    null = None
+    # kv_write: null pointers with tokens present
+    assert lib.pkv_kv_write(null, fake, fake, 4, fake, fake, _desc(), null, null) == 1
+    # kv_write: zero tokens is a no-op that succeeds without touching anything
+    assert lib.pkv_kv_write(null, null, null, 0, null, null, _desc(), null, null) == 0
+    # bad cache geometry
+    assert lib.pkv_kv_write(fake, fake, fake, 1, fake, fake, _desc(num_blocks=0), null, null) == 1
+    assert lib.pkv_kv_write(fake, fake, fake, 1, fake, fake, _desc(dtype=7), null, null) == 1
+    assert lib.pkv_kv_write(fake, fake, fake, 1, fake, fake, _desc(head_dim=12), null, null) == 2
+    # attention: heads not divisible, unsupported head dim / block size, capacity
+    args = lambda **kw: dict(dict(q=fake, kc=fake, vc=fake, bt=fake, mb=4, sl=fake, msl=64, S=2,
+                                  Hq=32, desc=_desc(), scale=0.1, part=0, ws=null, wsb=0,
+                                  out=fake), **kw)
+
+    def attn(**kw):
+        a = args(**kw)
+        return lib.pkv_paged_decode_attention(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"],
+                                              a["msl"], a["S"], a["Hq"], a["desc"],
+                                              ctypes.c_float(a["scale"]), a["part"], a["ws"],
+                                              a["wsb"], a["out"], null, null)
+
+    assert attn(Hq=30) == 1
+    assert attn(desc=_desc(head_dim=64)) == 2
+    assert attn(desc=_desc(block_size=8), msl=32) == 2
+    assert attn(msl=65) == 1  # beyond 4 blocks x 16 slots
+    assert attn(part=24) == 1
+    assert attn(q=null) == 1
+    assert attn(S=0) == 0
+    assert attn(scale=float("nan")) == 1
+    assert attn(Hq=8 * 65) == 2  # group of 65 query heads per KV head
+    # split mode without a workspace
+    assert attn(mb=300, msl=4097) == 3
+    # copy_blocks
+    assert lib.pkv_copy_blocks(fake, fake, _desc(), null, 3, null, null) == 1
+    assert lib.pkv_copy_blocks(null, null, _desc(), null, 0, null, null) == 0
+    assert lib.pkv_copy_blocks(fake, fake, _desc(), fake, -1, null, null) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIBRARY", str(tmp_path / "absent.so"))
+    with pytest.raises(_lib.PKVError):
+        _lib.load()

@@ -164,6 +164,37 @@ PKV_API pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache
                                       size_t workspace_bytes, void* out, int32_t* err_flag,
                                       void* stream);
 
+/* Size of the fixed device scratch of pkv_paged_decode_attention_fixed_scratch. */
+#define PKV_FIXED_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * pkv_paged_decode_attention for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * whose host application owns every GPU allocation (a server that hands its
+ * plugins only pre-registered buffers, or a runtime with its own pool and a
+ * fixed budget), where a cudaMalloc of their own could fail, fragment the
+ * host's pool or synchronise the device at the wrong time.
+ *
+ * Same arguments, results and errors as pkv_paged_decode_attention, minus
+ * the workspace: split-mode scratch comes from a fixed array of
+ * PKV_FIXED_SCRATCH_BYTES compiled into the library, present on every GPU
+ * that loads the library until the process exits.  The call allocates
+ * nothing.  A request whose scratch need (pkv_decode_workspace_bytes)
+ * exceeds PKV_FIXED_SCRATCH_BYTES returns PKV_ERR_WORKSPACE_TOO_SMALL and
+ * enqueues nothing.  The array's device address is looked up once per
+ * device, on that device's first call needing scratch, with the caller's
+ * current device (which must own `stream` and the buffers); make that first
+ * call before any stream capture.  All calls share the one array: calls whose
+ * kernels can overlap on the GPU (other streams, other host threads) race on
+ * it, so order them on one stream.  Its contents carry over between calls
+ * and need no clearing.
+ */
+PKV_API pkv_status pkv_paged_decode_attention_fixed_scratch(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+    int32_t num_q_heads, pkv_cache_desc c, float scale, int32_t partition_size, void* out,
+    int32_t* err_flag, void* stream);
+
 /*
  * Copy whole physical blocks, for copy-on-write of a shared block.
  *

@@ -314,7 +314,11 @@ def run_pkv(args, rank, world, local_rank):
         pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
                      dev["v_cache"], err_flag=err)
 
-    launches_per_step = 1 + (1 if has_cow else 0) + 1 + (1 if split else 0)
+    # kv_write, copy_blocks when pairs exist, the attention kernel, and the
+    # merge kernel (always in automatic mode; with explicit partitions only
+    # when a sequence spans several)
+    merges = 1 if (args.partition_size == 0 or split) else 0
+    launches_per_step = 1 + (1 if has_cow else 0) + 1 + merges
     for _ in range(max(3, args.warmup)):
         write()
         attention()
@@ -417,8 +421,8 @@ def run_pkv(args, rank, world, local_rank):
         return
     hbm, kind = measured_peaks()
     achieved = a_bytes / (attn_ms * 1e-3) / 1e9
-    source = os.path.join(ROOT, "paged_kv_cache_242_gb300", "csrc", "decode_attention.cu")
-    roofline = {"kernel": "paged_decode_attention (partition kernel + merge kernel)",
+    source = os.path.join(ROOT, "paged_kv_cache_242_gb300", "csrc", "decode_stream.cu")
+    roofline = {"kernel": "paged_decode_attention (streaming kernel + merge kernel)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_kind": f"{kind} (burst copy)",
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),

@@ -1,0 +1,427 @@
+// Streaming paged decode attention: a persistent grid with one CTA of eight
+// warps per SM, each warp an independent TMA pipeline.
+//
+// What it computes is the same as the partition kernel (decode_attention.cu):
+// for every sequence and query head, softmax(scale * q K^T) V over the
+// sequence's paged keys and values, block by block with the running max /
+// running sum of Eq. (4) of "Serving Language Models Within a Memory Budget"
+// (vLLM PagedAttention & continuous batching, "PagedAttention": the kernel
+// scores the query against one block, then the next, and combines them).
+//
+// Work split.  All (sequence, KV head) segments are cut into 16-token tiles
+// (a whole block at block size 16, half a block at 32) and laid end to end in
+// (sequence, head, tile) order.  Warp w of the grid takes the contiguous
+// range [w * per, (w + 1) * per) of that order, per = ceil(tiles / warps), so
+// every warp streams the same number of bytes and the grid finishes together
+// whatever the mix of lengths.  A warp that covers a whole segment writes the
+// final output; a warp whose range cuts a segment writes that segment's
+// partial (max, sum, weighted sum) statistics, which the merge kernel
+// combines by the same Eq. (4) rule.
+//
+// Pipeline.  Each warp owns three 8 KiB shared-memory stages (K and V of one
+// tile, two 64-column boxes each, 128-byte swizzle).  Lane 0 issues the TMA
+// loads of tile k + 3 as soon as the warp has finished tile k, so three
+// tiles per warp and 24 tiles per SM are always in flight; block-table
+// entries are fetched 32 at a time by the whole warp.  The per-tile math is
+// attend_block (decode_tile.cuh): mma.sync Q K^T, fp32 online softmax in the
+// log2 domain, mma.sync P V.
+//
+// The prologue of every CTA scans the sequence lengths into a prefix of tile
+// counts held in shared memory (up to 4096 sequences); CTA 0 also stores it
+// in the workspace for the merge kernel.
+#include "decode_tile.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kStageBytes = 4 * kTileTokens * 128;  // K and V, two halves each: 8 KiB
+constexpr int kHalf = kTileTokens * 128;             // one 64-column box of 16 rows
+constexpr int kRingBytes = kStreamWarps * kStages * kStageBytes;
+constexpr int kThreads = kStreamWarps * 32;
+
+struct alignas(8) StreamControl {
+    uint64_t full[kStreamWarps][kStages];
+    int32_t valid[kStreamWarps][kStages];
+    int32_t warp_total[kStreamWarps];
+};
+
+// Position of one tile in the (sequence, head, tile) order.
+struct Cursor {
+    int s;   // sequence
+    int h;   // KV head
+    int i;   // tile within the segment
+    int nt;  // tiles in the segment
+};
+
+__device__ __forceinline__ void cursor_advance(Cursor& c, const int32_t* prefix, int num_seqs,
+                                               int num_kv_heads) {
+    if (++c.i < c.nt) return;
+    c.i = 0;
+    if (++c.h < num_kv_heads) return;
+    c.h = 0;
+    do {
+        ++c.s;
+    } while (c.s < num_seqs && prefix[c.s + 1] == prefix[c.s]);
+    c.nt = c.s < num_seqs ? prefix[c.s + 1] - prefix[c.s] : 1;
+}
+
+// Locate global tile index t (0 <= t < total tiles).
+__device__ __forceinline__ Cursor cursor_at(int64_t t, const int32_t* prefix, int num_seqs,
+                                            int num_kv_heads) {
+    // largest s with num_kv_heads * prefix[s] <= t
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(prefix[mid]) * num_kv_heads <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    Cursor c;
+    c.s = lo;
+    c.nt = prefix[lo + 1] - prefix[lo];
+    const int64_t rem = t - static_cast<int64_t>(prefix[lo]) * num_kv_heads;
+    c.h = static_cast<int>(rem / c.nt);
+    c.i = static_cast<int>(rem - static_cast<int64_t>(c.h) * c.nt);
+    return c;
+}
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_stream_kernel(const __grid_constant__ CUtensorMap k_map,
+                               const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    StreamControl* ctl = reinterpret_cast<StreamControl*>(ring + kRingBytes);
+    int32_t* prefix = reinterpret_cast<int32_t*>(ctl + 1);  // [S + 1]
+    int32_t* lens = prefix + a.num_seqs + 1;                // [S]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = a.num_seqs;
+    const int H = a.num_kv_heads;
+
+    // ---- prologue: tile-count prefix over the sequences ---------------------
+    {
+        const int per_thread = (S + kThreads - 1) / kThreads;  // <= 16
+        const int base = threadIdx.x * per_thread;
+        int sum = 0;
+        for (int k = 0; k < per_thread; ++k) {
+            const int idx = base + k;
+            if (idx < S) {
+                const int n = clamped_len(a, idx, blockIdx.x == 0);
+                lens[idx] = n;
+                sum += (n + kTileTokens - 1) / kTileTokens;
+            }
+        }
+        // block-wide exclusive scan of the per-thread sums
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane == 31) ctl->warp_total[warp] = incl;
+        if (threadIdx.x == 0) {
+            for (int w = 0; w < kStreamWarps; ++w) {
+                for (int st = 0; st < kStages; ++st) mbar_init(smem_addr(&ctl->full[w][st]), 1);
+            }
+            fence_barrier_init();
+        }
+        __syncthreads();
+        int offset = 0;
+        for (int w = 0; w < warp; ++w) offset += ctl->warp_total[w];
+        int run = offset + incl - sum;  // exclusive prefix of this thread's first element
+        for (int k = 0; k < per_thread; ++k) {
+            const int idx = base + k;
+            if (idx < S) {
+                prefix[idx] = run;
+                run += (lens[idx] + kTileTokens - 1) / kTileTokens;
+            }
+        }
+        if (threadIdx.x == kThreads - 1) {
+            int total = 0;
+            for (int w = 0; w < kStreamWarps; ++w) total += ctl->warp_total[w];
+            prefix[S] = total;
+        }
+        __syncthreads();
+        if (blockIdx.x == 0) {
+            for (int idx = threadIdx.x; idx <= S; idx += kThreads) a.ws_prefix[idx] = prefix[idx];
+        }
+    }
+
+    // ---- this warp's share of the tiles --------------------------------------
+    const int64_t total_tiles = static_cast<int64_t>(prefix[S]) * H;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + warp;
+    const int64_t per = total_tiles > 0 ? (total_tiles + a.num_warps - 1) / a.num_warps : 1;
+    const int64_t t0 = gw * per;
+    const int64_t t1 = min(t0 + per, total_tiles);
+    if (t0 >= t1) return;
+    const int count = static_cast<int>(t1 - t0);
+
+    uint8_t* my_ring = ring + warp * kStages * kStageBytes;
+    const int g = a.group;
+    const int row0 = lane >> 2;
+    const int quad = lane & 3;
+
+    // ---- issue side: cursor, block-table window ------------------------------
+    Cursor iss = cursor_at(t0, prefix, S, H);
+    int win_s = -1, win_base = 0, win_id = -1;
+    int issued = 0;
+    auto issue = [&](int k) {
+        issued = k + 1;
+        const int st = k % kStages;
+        const int blk = (iss.i * kTileTokens) / BS;  // block of the sequence
+        if (iss.s != win_s || blk < win_base || blk >= win_base + 32) {
+            win_s = iss.s;
+            win_base = blk;
+            const int nblocks = (lens[iss.s] + BS - 1) / BS;
+            const int e = win_base + lane;
+            win_id = e < nblocks ? __ldg(a.block_tables + static_cast<size_t>(iss.s) *
+                                                               a.max_blocks_per_seq + e)
+                                 : -1;
+        }
+        const int id = __shfl_sync(0xffffffffu, win_id, blk - win_base);
+        if (lane == 0) {
+            const bool ok = id >= 0 && id < a.num_blocks;
+            const uint32_t full = smem_addr(&ctl->full[warp][st]);
+            ctl->valid[warp][st] = ok ? 1 : 0;
+            if (ok) {
+                const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
+                const uint32_t vt = kt + 2 * kHalf;
+                const int row = (iss.i * kTileTokens) % BS;
+                fence_proxy_async_shared();  // earlier generic reads of this stage
+                mbar_arrive_expect_tx(full, kStageBytes);
+                tma_load_4d(kt, &k_map, full, 0, row, iss.h, id);
+                tma_load_4d(kt + kHalf, &k_map, full, 64, row, iss.h, id);
+                tma_load_4d(vt, &v_map, full, 0, row, iss.h, id);
+                tma_load_4d(vt + kHalf, &v_map, full, 64, row, iss.h, id);
+            } else {
+                report(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+                mbar_arrive(full);
+            }
+        }
+        cursor_advance(iss, prefix, S, H);
+    };
+
+    if (lane == 0) {
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&v_map);
+    }
+    const int prologue = count < kStages ? count : kStages;
+    for (int k = 0; k < prologue; ++k) issue(k);
+
+    // ---- consume side ----------------------------------------------------------
+    Cursor cur = cursor_at(t0, prefix, S, H);
+    bool seg_from_start = cur.i == 0;
+    uint32_t qa[8][4];
+    float o[16][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    auto reset = [&]() {
+        const T* q_rows = static_cast<const T*>(a.q) +
+                          (static_cast<size_t>(cur.s) * a.num_q_heads + static_cast<size_t>(cur.h) * g) *
+                              kHeadDim;
+        load_q_fragments<T>(qa, q_rows, g, lane);
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    };
+
+    // Write the finished segment `seg` (its whole range, or this warp's part).
+    auto flush = [&](const Cursor& seg, bool whole) {
+        float s0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        float s1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        const size_t qrow = static_cast<size_t>(seg.s) * a.num_q_heads + static_cast<size_t>(seg.h) * g;
+        if (whole) {
+            const float inv0 = s0 > 0.f ? 1.f / s0 : 0.f;
+            const float inv1 = s1 > 0.f ? 1.f / s1 : 0.f;
+            T* out = static_cast<T*>(a.out);
+#pragma unroll
+            for (int nd = 0; nd < 16; ++nd) {
+                const int col = nd * 8 + quad * 2;
+                if (row0 < g)
+                    *reinterpret_cast<uint32_t*>(out + (qrow + row0) * kHeadDim + col) =
+                        Mma<T>::pack(o[nd][0] * inv0, o[nd][1] * inv0);
+                if (row0 + 8 < g)
+                    *reinterpret_cast<uint32_t*>(out + (qrow + row0 + 8) * kHeadDim + col) =
+                        Mma<T>::pack(o[nd][2] * inv1, o[nd][3] * inv1);
+            }
+        } else {
+            const int64_t pid = gw + static_cast<int64_t>(seg.s) * H + seg.h;
+            const size_t rbase = static_cast<size_t>(pid) * g;
+#pragma unroll
+            for (int nd = 0; nd < 16; ++nd) {
+                const int col = nd * 8 + quad * 2;
+                if (row0 < g)
+                    *reinterpret_cast<float2*>(a.ws_acc + (rbase + row0) * kHeadDim + col) =
+                        make_float2(o[nd][0], o[nd][1]);
+                if (row0 + 8 < g)
+                    *reinterpret_cast<float2*>(a.ws_acc + (rbase + row0 + 8) * kHeadDim + col) =
+                        make_float2(o[nd][2], o[nd][3]);
+            }
+            if (quad == 0) {
+                if (row0 < g) {
+                    a.ws_m[rbase + row0] = m0;
+                    a.ws_l[rbase + row0] = s0;
+                }
+                if (row0 + 8 < g) {
+                    a.ws_m[rbase + row0 + 8] = m1;
+                    a.ws_l[rbase + row0 + 8] = s1;
+                }
+            }
+        }
+    };
+
+    reset();
+    bool aborted = false;
+    for (int k = 0; k < count; ++k) {
+        const int st = k % kStages;
+        if (k > 0 && cur.i == 0) {  // a new segment starts with this tile
+            seg_from_start = true;
+            reset();
+        }
+        if (!mbar_wait(smem_addr(&ctl->full[warp][st]), (k / kStages) & 1)) {
+            report(a.err, PKV_DEVERR_TIMEOUT);
+            aborted = true;
+            break;
+        }
+        if (ctl->valid[warp][st]) {
+            const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
+            const int nvalid = min(kTileTokens, lens[cur.s] - cur.i * kTileTokens);
+            attend_block<T, kTileTokens, true>(kt, kt + 2 * kHalf, nvalid, qa, o, m0, m1, l0, l1,
+                                               a.scale_log2, lane);
+        }
+        __syncwarp();
+        if (k + kStages < count) issue(k + kStages);
+        const bool seg_ends = cur.i == cur.nt - 1 || k == count - 1;
+        if (seg_ends) flush(cur, seg_from_start && cur.i == cur.nt - 1);
+        cursor_advance(cur, prefix, S, H);
+    }
+    if (aborted && lane == 0) {
+        // do not leave while this warp's copies are still landing (bounded)
+        for (int st = 0; st < kStages && st < issued; ++st) {
+            const int last = ((issued - 1 - st) / kStages) * kStages + st;  // last use of st
+            mbar_wait(smem_addr(&ctl->full[warp][st]), (last / kStages) & 1);
+        }
+    }
+}
+
+// Merge of the partial statistics of segments cut by warp ranges (Eq. 4):
+// out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w, M = max_w m_w.
+// One CTA per (sequence, KV head) segment, one thread per output column.
+template <typename T>
+__global__ void __launch_bounds__(kHeadDim) merge_stream_kernel(const DecodeArgs a) {
+    const int j = blockIdx.x;  // segment = s * H + h
+    const int H = a.num_kv_heads;
+    const int s = j / H;
+    const int h = j - s * H;
+    const int d = threadIdx.x;
+    const int g = a.group;
+    const int p_s = a.ws_prefix[s];
+    const int nt = a.ws_prefix[s + 1] - p_s;
+    T* out = static_cast<T*>(a.out) + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g) * kHeadDim;
+    if (nt == 0) {  // empty sequence: zero output
+        for (int r = 0; r < g; ++r) out[r * kHeadDim + d] = Mma<T>::from_float(0.f);
+        return;
+    }
+    const int64_t total_tiles = static_cast<int64_t>(a.ws_prefix[a.num_seqs]) * H;
+    const int64_t per = (total_tiles + a.num_warps - 1) / a.num_warps;
+    const int64_t first = static_cast<int64_t>(p_s) * H + static_cast<int64_t>(h) * nt;
+    const int64_t w0 = first / per;
+    const int64_t w1 = (first + nt - 1) / per;
+    if (w0 == w1) return;  // one warp covered the segment and wrote the output
+    for (int r = 0; r < g; ++r) {
+        float big = -INFINITY;
+        for (int64_t w = w0; w <= w1; ++w) big = fmaxf(big, a.ws_m[(w + j) * g + r]);
+        float num = 0.f, den = 0.f;
+        if (big != -INFINITY) {
+            for (int64_t w = w0; w <= w1; ++w) {
+                const size_t row = static_cast<size_t>(w + j) * g + r;
+                const float wt = ex2(a.ws_m[row] - big);
+                den += wt * a.ws_l[row];
+                num += wt * a.ws_acc[row * kHeadDim + d];
+            }
+        }
+        out[r * kHeadDim + d] = Mma<T>::from_float(den > 0.f ? num / den : 0.f);
+    }
+}
+
+template <typename T, int BS>
+cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                const DecodeArgs& a, int ctas, cudaStream_t stream) {
+    const size_t smem = 1024 + kRingBytes + sizeof(StreamControl) +
+                        (2 * static_cast<size_t>(a.num_seqs) + 1) * sizeof(int32_t);
+    auto kernel = paged_decode_stream_kernel<T, BS>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    kernel<<<ctas, kThreads, smem, stream>>>(k_map, v_map, a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    merge_stream_kernel<T><<<a.num_seqs * a.num_kv_heads, kHeadDim, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool stream_supported(int num_seqs, int group, int block_size) {
+    return num_seqs >= 1 && num_seqs <= kStreamMaxSeqs && group >= 1 && group <= 16 &&
+           (block_size == 16 || block_size == 32) &&
+           1024 + kRingBytes + sizeof(StreamControl) + (2 * static_cast<size_t>(num_seqs) + 1) * 4 <=
+               232448;
+}
+
+// Rows of partial statistics: one per (partial id, query head of the group);
+// partial ids are (warp + segment) < warps + S * H_kv.  Without H_kv the
+// group is bounded by min(16, H_q).
+size_t stream_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads_or_0) {
+    const size_t warps = static_cast<size_t>(kStreamMaxCtas) * kStreamWarps;
+    size_t rows;
+    if (num_kv_heads_or_0 > 0) {
+        const size_t g = static_cast<size_t>(num_q_heads / num_kv_heads_or_0);
+        rows = (warps + static_cast<size_t>(num_seqs) * num_kv_heads_or_0) * g;
+    } else {
+        const size_t gmax = static_cast<size_t>(num_q_heads < 16 ? num_q_heads : 16);
+        rows = warps * gmax + static_cast<size_t>(num_seqs) * num_q_heads;
+    }
+    const size_t floats = rows * (kHeadDim + 2);
+    const size_t prefix = (static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t);
+    return floats * sizeof(float) + ((prefix + 255) / 256) * 256;
+}
+
+cudaError_t launch_paged_decode_stream(const CUtensorMap& k_map16, const CUtensorMap& v_map16,
+                                       DecodeArgs a, pkv_dtype dtype, int block_size,
+                                       cudaStream_t stream) {
+    int device = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (err != cudaSuccess) return err;
+    // enough CTAs for ~16 tiles per warp, at most one per SM
+    const int64_t max_tiles = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
+                              ((a.max_seq_len + kTileTokens - 1) / kTileTokens);
+    int64_t ctas = (max_tiles + kStreamWarps * 16 - 1) / (kStreamWarps * 16);
+    const int cap = sms < kStreamMaxCtas ? sms : kStreamMaxCtas;
+    if (ctas > cap) ctas = cap;
+    if (ctas < 1) ctas = 1;
+    a.num_warps = static_cast<int32_t>(ctas) * kStreamWarps;
+    // workspace layout: acc [rows][128], m [rows], l [rows], prefix [S + 1]
+    const size_t rows = (static_cast<size_t>(a.num_warps) +
+                         static_cast<size_t>(a.num_seqs) * a.num_kv_heads) * a.group;
+    float* ws = a.ws_acc;
+    a.ws_m = ws + rows * kHeadDim;
+    a.ws_l = a.ws_m + rows;
+    a.ws_prefix = reinterpret_cast<int32_t*>(a.ws_l + rows);
+    const bool bf16 = dtype == PKV_BF16;
+    if (block_size == 16)
+        return bf16 ? launch_stream_typed<__nv_bfloat16, 16>(k_map16, v_map16, a, (int)ctas, stream)
+                    : launch_stream_typed<__half, 16>(k_map16, v_map16, a, (int)ctas, stream);
+    return bf16 ? launch_stream_typed<__nv_bfloat16, 32>(k_map16, v_map16, a, (int)ctas, stream)
+                : launch_stream_typed<__half, 32>(k_map16, v_map16, a, (int)ctas, stream);
+}
+
+}  // namespace pkv

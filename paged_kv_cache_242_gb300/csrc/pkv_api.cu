@@ -44,9 +44,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A 4-D view of one pool, {head_dim, block_size, num_kv_heads, num_blocks}
-// (innermost first), tiled in boxes of {64, block_size, 1, 1} with the
-// 128-byte swizzle: one box is one half (64 columns) of a (block, head) tile.
-bool encode_pool(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
+// (innermost first), tiled in boxes of {64, box_rows, 1, 1} with the
+// 128-byte swizzle: one box is one half (64 columns) of box_rows token rows
+// of a (block, head) tile (box_rows = block_size, or 16 for streamed tiles).
+bool encode_pool(CUtensorMap* map, const void* base, const pkv_cache_desc& c, int box_rows) {
     auto encode = tensor_map_encoder();
     if (encode == nullptr) return false;
     const cuuint64_t row = static_cast<cuuint64_t>(c.head_dim) * 2;
@@ -54,7 +55,7 @@ bool encode_pool(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
                           static_cast<cuuint64_t>(c.num_kv_heads),
                           static_cast<cuuint64_t>(c.num_blocks)};
     cuuint64_t strides[3] = {row, row * c.block_size, row * c.block_size * c.num_kv_heads};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(c.block_size), 1, 1};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
     cuuint32_t elem[4] = {1, 1, 1, 1};
     const CUtensorMapDataType type =
         c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -137,7 +138,14 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
     if (num_seqs <= 0 || num_q_heads <= 0) return 0;
     const int32_t part = effective_partition(max_seq_len, block_size, partition_size);
     if (part <= 0) return 0;
-    return workspace_for(num_seqs, num_q_heads, partitions_for(max_seq_len, part));
+    size_t need = workspace_for(num_seqs, num_q_heads, partitions_for(max_seq_len, part));
+    // automatic mode streams when the shape allows it (the group size is not
+    // known here, so size for the larger of the two layouts)
+    if (partition_size == 0 && pkv::stream_supported(num_seqs, 1, block_size)) {
+        const size_t stream = pkv::stream_workspace_bytes(num_seqs, num_q_heads, 0);
+        if (stream > need) need = stream;
+    }
+    return need;
 }
 
 pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -165,22 +173,30 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
         !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PKV_ERR_INVALID_ARG;
 
+    const int32_t group = num_q_heads / c.num_kv_heads;
+    const bool streaming =
+        partition_size == 0 && pkv::stream_supported(num_seqs, group, c.block_size);
     const int32_t part = effective_partition(max_seq_len, c.block_size, partition_size);
     const int32_t max_parts = partitions_for(max_seq_len, part);
-    const size_t need = workspace_for(num_seqs, num_q_heads, max_parts);
+    const size_t need = streaming ? pkv::stream_workspace_bytes(num_seqs, num_q_heads, c.num_kv_heads)
+                                  : workspace_for(num_seqs, num_q_heads, max_parts);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
         return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (need > 0 && !aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
 
     CUtensorMap k_map, v_map;
-    if (!encode_pool(&k_map, k_cache, c) || !encode_pool(&v_map, v_cache, c)) return PKV_ERR_CUDA;
+    const int box_rows = streaming ? pkv::kTileTokens : c.block_size;
+    if (!encode_pool(&k_map, k_cache, c, box_rows) || !encode_pool(&v_map, v_cache, c, box_rows))
+        return PKV_ERR_CUDA;
 
     pkv::DecodeArgs a{};
     a.q = q;
     a.out = out;
     a.block_tables = block_tables;
     a.seq_lens = seq_lens;
-    if (need > 0) {
+    if (streaming) {
+        a.ws_acc = static_cast<float*>(workspace);  // laid out by the stream launcher
+    } else if (need > 0) {
         const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
         float* ws = static_cast<float*>(workspace);
         a.ws_acc = ws;
@@ -192,14 +208,17 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = c.num_kv_heads;
-    a.group = num_q_heads / c.num_kv_heads;
+    a.group = group;
     a.num_blocks = c.num_blocks;
     a.partition_size = part;
     a.max_partitions = max_parts;
     a.max_seq_len = max_seq_len;
     a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     cudaError_t e =
-        pkv::launch_paged_decode(k_map, v_map, a, c.dtype, c.block_size, static_cast<cudaStream_t>(stream));
+        streaming ? pkv::launch_paged_decode_stream(k_map, v_map, a, c.dtype, c.block_size,
+                                                    static_cast<cudaStream_t>(stream))
+                  : pkv::launch_paged_decode(k_map, v_map, a, c.dtype, c.block_size,
+                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -33,7 +33,23 @@ struct DecodeArgs {
     int32_t max_partitions;     // ceil(max_seq_len / partition_size), >= 1
     int32_t max_seq_len;
     float scale_log2;           // softmax scale * log2(e)
+    int32_t* ws_prefix;         // stream mode: [S + 1] tile prefix over sequences
+    int32_t num_warps;          // stream mode: warps in the grid
 };
+
+constexpr int kStreamWarps = 8;         // warps per CTA of the streaming kernel
+constexpr int kStreamMaxCtas = 160;     // cap of its grid (one CTA per SM)
+constexpr int kStreamMaxSeqs = 4096;    // sequences whose prefix fits shared memory
+constexpr int kTileTokens = 16;         // tokens per streamed tile
+
+// Streaming mode: every warp of a persistent grid takes an equal share of
+// all 16-token tiles in (sequence, KV head, tile) order; shares that cut a
+// (sequence, head) segment leave partial statistics for the merge kernel.
+bool stream_supported(int num_seqs, int group, int block_size);
+size_t stream_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads_or_0);
+cudaError_t launch_paged_decode_stream(const CUtensorMap& k_map16, const CUtensorMap& v_map16,
+                                       DecodeArgs args, pkv_dtype dtype, int block_size,
+                                       cudaStream_t stream);
 
 // Launch the split (or single-pass, when max_partitions == 1) decode
 // kernel and, in split mode, the merge kernel.

@@ -57,9 +57,17 @@ def test_partition_and_workspace_queries(lib):
     assert lib.pkv_decode_partition_size(300, 16, 64) == 64
     assert lib.pkv_decode_partition_size(300, 16, 24) == -1  # not a multiple of the block size
     assert lib.pkv_decode_partition_size(32768, 16, 1 << 20) == 32768
-    # 64 seqs x 32 heads x ceil(4097/512)=9 partitions x (128 + 2) floats
-    assert lib.pkv_decode_workspace_bytes(64, 32, 128, 4097, 16, 0) == 64 * 32 * 9 * 130 * 4
-    assert lib.pkv_decode_workspace_bytes(5, 8, 128, 511, 16, 0) == 0
+    # explicit partitions: 64 seqs x 32 heads x ceil(4097/512)=9 partitions x (128 + 2) floats
+    assert lib.pkv_decode_workspace_bytes(64, 32, 128, 4097, 16, 512) == 64 * 32 * 9 * 130 * 4
+    assert lib.pkv_decode_workspace_bytes(5, 8, 128, 511, 16, 512) == 0  # single pass
+    # automatic mode: at least the streaming layout's bound (1280 warps x 16 rows
+    # + S x H_q rows of 130 floats, plus the tile prefix)
+    auto = lib.pkv_decode_workspace_bytes(64, 32, 128, 4097, 16, 0)
+    assert auto >= (1280 * 16 + 64 * 32) * 130 * 4 + 65 * 4
+    assert auto >= 64 * 32 * 9 * 130 * 4
+    assert lib.pkv_decode_workspace_bytes(5, 8, 128, 511, 16, 0) > 0
+    # beyond 4096 sequences automatic mode falls back to partitions
+    assert lib.pkv_decode_workspace_bytes(5000, 8, 128, 511, 16, 0) == 0
 
 
 def _desc(**kw):

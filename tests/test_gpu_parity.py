@@ -225,12 +225,39 @@ def test_shared_prefix_equals_private_copy_bitwise():
     assert torch.equal(out_private, out_shared)
 
 
+@pytest.mark.parametrize("B", [16, 32])
+def test_stream_many_short_and_empty_sequences(B):
+    """Streaming split over many segments: warp ranges cut segments anywhere."""
+    g = torch.Generator().manual_seed(30 + B)
+    context = torch.randint(0, 300, (300,), generator=g).tolist()
+    step = _custom(context, 16, 4, B, "bfloat16", seed=31)
+    # a third of the sequences are empty (attended length 0)
+    for s in range(0, 300, 3):
+        step.seq_lens[s] = 0
+    _full_step_parity(step, partition_sizes=(0, 64))
+
+
+def test_stream_limit_and_partition_fallback():
+    """4096 sequences stream; 4097 fall back to partitions; both match."""
+    for S in (4096, 4097):
+        g = torch.Generator().manual_seed(S)
+        context = torch.randint(0, 40, (S,), generator=g).tolist()
+        step = _custom(context, 8, 2, 16, "float16", seed=S)
+        _full_step_parity(step, partition_sizes=(0,))
+
+
+def test_stream_single_long_sequence_many_partials():
+    """One 64k-token sequence over every warp: the merge combines ~1000 partials."""
+    step = _custom([65535], 8, 1, 32, "bfloat16", seed=33, pool_factor=1.0)
+    _full_step_parity(step, partition_sizes=(0,))
+
+
 def test_split_size_invariance():
     step = _custom([3000, 4000, 2500], 32, 8, 16, "bfloat16", seed=18)
     kc, vc = bits(step.k_cache), bits(step.v_cache)
     ref, _, _ = oracle_step(step, kc, vc)
     outs = []
-    for part in (16, 128, 512, 2048, 8192):
+    for part in (0, 16, 128, 512, 2048, 8192):
         dev = to_device(step)
         outs.append(gpu_step(step, dev, partition_size=part))
         assert_attention_close(outs[-1], ref, f"P={part}")

@@ -327,8 +327,13 @@ def run_pkv(args, rank, world, local_rank):
         torch.distributed.barrier()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    # Events around the attention call on every 8th step only: an event
+    # recorded between two kernels stops them from overlapping their launch
+    # (programmatic dependent launch), so the other steps run undisturbed.
+    sample_every = 8
+    sampled = list(range(0, K, sample_every))
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for i in sampled}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(device.index if device.index is not None else 0)
     clocks.start()
@@ -337,16 +342,19 @@ def run_pkv(args, rank, world, local_rank):
     start.record(stream)
     for i in range(K):
         write()
-        ev[i][0].record(stream)
+        pair = ev.get(i)
+        if pair is not None:
+            pair[0].record(stream)
         attention()
-        ev[i][1].record(stream)
+        if pair is not None:
+            pair[1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     total_ms = start.elapsed_time(end)
-    attn_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev.values()) / len(ev)
     assert int(err.item()) == 0, f"device error flag {int(err.item())}"
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K

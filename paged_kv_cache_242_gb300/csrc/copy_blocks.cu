@@ -20,6 +20,8 @@ constexpr int kVecsPerCta = kCopyThreads * kCopyUnroll;
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int64_t* __restrict__ pairs,
     int64_t vecs_per_block, int32_t num_blocks, int32_t* err) {
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int64_t pair = blockIdx.x;
     const int64_t src = __ldg(pairs + 2 * pair);
     const int64_t dst = __ldg(pairs + 2 * pair + 1);
@@ -61,10 +63,9 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_des
         static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
     const int64_t chunks = (vecs_per_block + kVecsPerCta - 1) / kVecsPerCta;
     dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(chunks));
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs, vecs_per_block,
-        c.num_blocks, err);
-    return cudaGetLastError();
+    return launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, stream,
+                      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs,
+                      vecs_per_block, c.num_blocks, err);
 }
 
 }  // namespace pkv

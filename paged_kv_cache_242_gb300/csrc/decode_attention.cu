@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int n = clamped_len(a, s, p == 0 && h == 0 && threadIdx.x == 0);
     const int P = a.partition_size;
     const int np_s = n > 0 ? (n + P - 1) / P : 1;
@@ -251,6 +253,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 template <typename T>
 __global__ void __launch_bounds__(kHeadDim) merge_partitions_kernel(const DecodeArgs a) {
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int i = blockIdx.x;  // query head
     const int s = blockIdx.y;
     const int d = threadIdx.x;
@@ -286,12 +290,10 @@ cudaError_t launch_typed(const CUtensorMap& k_map, const CUtensorMap& v_map, con
     if (err != cudaSuccess) return err;
     dim3 grid(static_cast<unsigned>(a.max_partitions), static_cast<unsigned>(a.num_kv_heads),
               static_cast<unsigned>(a.num_seqs));
-    kernel<<<grid, kDecodeThreads, smem, stream>>>(k_map, v_map, a);
-    err = cudaGetLastError();
+    err = launch_pdl(kernel, grid, dim3(kDecodeThreads), smem, stream, k_map, v_map, a);
     if (err != cudaSuccess || a.max_partitions <= 1) return err;
     dim3 mgrid(static_cast<unsigned>(a.num_q_heads), static_cast<unsigned>(a.num_seqs));
-    merge_partitions_kernel<T><<<mgrid, kHeadDim, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(merge_partitions_kernel<T>, mgrid, dim3(kHeadDim), 0, stream, a);
 }
 
 template <typename T, int BS>

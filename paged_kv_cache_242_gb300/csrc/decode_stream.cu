@@ -18,11 +18,11 @@
 // partial (max, sum, weighted sum) statistics, which the merge kernel
 // combines by the same Eq. (4) rule.
 //
-// Pipeline.  Each warp owns three 8 KiB shared-memory stages (K and V of one
-// tile, two 64-column boxes each, 128-byte swizzle).  Lane 0 issues the TMA
-// loads of tile k + 3 as soon as the warp has finished tile k, so three
-// tiles per warp and 24 tiles per SM are always in flight; block-table
-// entries are fetched 32 at a time by the whole warp.  The per-tile math is
+// Pipeline.  Each warp owns kStreamStages (3) 8 KiB shared-memory stages
+// (K and V of one tile, two 64-column boxes each, 128-byte swizzle).  Lane 0
+// issues the TMA loads of tile k + 3 as soon as the warp has finished tile k,
+// so three tiles per warp and 24 per SM are in flight or being consumed;
+// block-table entries are fetched 32 at a time by the whole warp.  The per-tile math is
 // attend_block (decode_tile.cuh): mma.sync Q K^T, fp32 online softmax in the
 // log2 domain, mma.sync P V.
 //
@@ -34,7 +34,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = kStreamStages;
 constexpr int kStageBytes = 4 * kTileTokens * 128;  // K and V, two halves each: 8 KiB
 constexpr int kHalf = kTileTokens * 128;             // one 64-column box of 16 rows
 constexpr int kRingBytes = kStreamWarps * kStages * kStageBytes;
@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int S = a.num_seqs;
     const int H = a.num_kv_heads;
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
 
     // ---- prologue: tile-count prefix over the sequences ---------------------
     {
@@ -312,20 +314,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge of the partial statistics of segments cut by warp ranges (Eq. 4):
 // out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w, M = max_w m_w.
-// One CTA per (sequence, KV head) segment, one thread per output column.
+// One warp per (segment, query head of the group); lanes take partials 32 at
+// a time for the statistics and 4 output columns each for the weighted sum,
+// so every load of a warp is issued together.
+constexpr int kMergeWarps = 4;
+
 template <typename T>
-__global__ void __launch_bounds__(kHeadDim) merge_stream_kernel(const DecodeArgs a) {
-    const int j = blockIdx.x;  // segment = s * H + h
-    const int H = a.num_kv_heads;
-    const int s = j / H;
-    const int h = j - s * H;
-    const int d = threadIdx.x;
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const DecodeArgs a) {
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int g = a.group;
+    const int H = a.num_kv_heads;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    if (item >= static_cast<int64_t>(a.num_seqs) * H * g) return;
+    const int lane = threadIdx.x & 31;
+    const int r = static_cast<int>(item % g);
+    const int64_t j = item / g;  // segment = s * H + h
+    const int s = static_cast<int>(j / H);
+    const int h = static_cast<int>(j - static_cast<int64_t>(s) * H);
     const int p_s = a.ws_prefix[s];
     const int nt = a.ws_prefix[s + 1] - p_s;
-    T* out = static_cast<T*>(a.out) + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g) * kHeadDim;
+    T* orow = static_cast<T*>(a.out) +
+              (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g + r) * kHeadDim;
+    uint2* ocol = reinterpret_cast<uint2*>(orow + lane * 4);  // this lane's 4 columns
+    const int col = lane * 4;
     if (nt == 0) {  // empty sequence: zero output
-        for (int r = 0; r < g; ++r) out[r * kHeadDim + d] = Mma<T>::from_float(0.f);
+        *ocol = make_uint2(0u, 0u);
         return;
     }
     const int64_t total_tiles = static_cast<int64_t>(a.ws_prefix[a.num_seqs]) * H;
@@ -334,20 +348,55 @@ __global__ void __launch_bounds__(kHeadDim) merge_stream_kernel(const DecodeArgs
     const int64_t w0 = first / per;
     const int64_t w1 = (first + nt - 1) / per;
     if (w0 == w1) return;  // one warp covered the segment and wrote the output
-    for (int r = 0; r < g; ++r) {
-        float big = -INFINITY;
-        for (int64_t w = w0; w <= w1; ++w) big = fmaxf(big, a.ws_m[(w + j) * g + r]);
-        float num = 0.f, den = 0.f;
-        if (big != -INFINITY) {
-            for (int64_t w = w0; w <= w1; ++w) {
-                const size_t row = static_cast<size_t>(w + j) * g + r;
-                const float wt = ex2(a.ws_m[row] - big);
-                den += wt * a.ws_l[row];
-                num += wt * a.ws_acc[row * kHeadDim + d];
-            }
+    const int np = static_cast<int>(w1 - w0 + 1);
+    const size_t row0 = static_cast<size_t>(w0 + j) * g + r;  // partial p is row0 + p * g
+
+    // pass 1: M = max m_p and L = sum 2^(m_p - M) l_p, online over chunks of 32
+    float big = -INFINITY, den = 0.f;
+    for (int base = 0; base < np; base += 32) {
+        const int p = base + lane;
+        float m = -INFINITY, l = 0.f;
+        if (p < np) {
+            m = a.ws_m[row0 + static_cast<size_t>(p) * g];
+            l = a.ws_l[row0 + static_cast<size_t>(p) * g];
         }
-        out[r * kHeadDim + d] = Mma<T>::from_float(den > 0.f ? num / den : 0.f);
+        float cm = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        const float nb = fmaxf(big, cm);
+        float c = (m == -INFINITY) ? 0.f : ex2(m - nb) * l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        den = (big == -INFINITY ? 0.f : den * ex2(big - nb)) + c;
+        big = nb;
     }
+    if (big == -INFINITY || !(den > 0.f)) {
+        *ocol = make_uint2(0u, 0u);
+        return;
+    }
+    // pass 2: sum_p 2^(m_p - M) acc_p over this lane's four columns
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = 0; base < np; base += 32) {
+        const int p = base + lane;
+        float wt = 0.f;
+        if (p < np) {
+            const float m = a.ws_m[row0 + static_cast<size_t>(p) * g];
+            wt = m == -INFINITY ? 0.f : ex2(m - big);
+        }
+        const int cnt = min(32, np - base);
+#pragma unroll 4
+        for (int q = 0; q < cnt; ++q) {
+            const float wq = __shfl_sync(0xffffffffu, wt, q);
+            const float4 v = *reinterpret_cast<const float4*>(
+                a.ws_acc + (row0 + static_cast<size_t>(base + q) * g) * kHeadDim + col);
+            acc.x += wq * v.x;
+            acc.y += wq * v.y;
+            acc.z += wq * v.z;
+            acc.w += wq * v.w;
+        }
+    }
+    const float inv = 1.f / den;
+    *ocol = make_uint2(Mma<T>::pack(acc.x * inv, acc.y * inv), Mma<T>::pack(acc.z * inv, acc.w * inv));
 }
 
 template <typename T, int BS>
@@ -359,11 +408,12 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kernel<<<ctas, kThreads, smem, stream>>>(k_map, v_map, a);
-    err = cudaGetLastError();
+    err = launch_pdl(kernel, dim3(ctas), dim3(kThreads), smem, stream, k_map, v_map, a);
     if (err != cudaSuccess) return err;
-    merge_stream_kernel<T><<<a.num_seqs * a.num_kv_heads, kHeadDim, 0, stream>>>(a);
-    return cudaGetLastError();
+    const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.group;
+    const int64_t blocks = (items + kMergeWarps - 1) / kMergeWarps;
+    return launch_pdl(merge_stream_kernel<T>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kMergeWarps * 32), 0, stream, a);
 }
 
 }  // namespace

@@ -7,37 +7,41 @@
 // One thread moves one 16-byte vector of a (token, KV head) row of K and
 // the matching vector of V; rows are head_dim * 2 bytes, contiguous on both
 // sides, so loads and stores are fully coalesced.  The kernel is bound by
-// launch latency at decode sizes (tens to hundreds of KiB per call).
+// launch latency at decode sizes (tens to hundreds of KiB per call); index
+// arithmetic stays in 32 bits unless the pool or the batch needs more.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
+template <typename I>
 __global__ void __launch_bounds__(256) kv_write_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v,
     const int64_t* __restrict__ slot_mapping, int32_t num_tokens, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int32_t num_kv_heads, int32_t block_size, int32_t chunks,
     int64_t num_slots, int32_t* err) {
-    const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * chunks;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-         idx += stride) {
-        const int64_t row = idx / chunks;  // token * num_kv_heads + head
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
+    const I total = static_cast<I>(num_tokens) * num_kv_heads * chunks;
+    const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+    for (I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const I row = idx / chunks;  // token * num_kv_heads + head
         const int32_t c = static_cast<int32_t>(idx - row * chunks);
-        const int64_t t = row / num_kv_heads;
+        const I t = row / num_kv_heads;
         const int32_t h = static_cast<int32_t>(row - t * num_kv_heads);
+        const uint4 kv = __ldg(k + idx);
+        const uint4 vv = __ldg(v + idx);
         const int64_t slot = __ldg(slot_mapping + t);
         if (slot < 0) continue;  // padding token
         if (slot >= num_slots) {
             if (h == 0 && c == 0) report(err, PKV_DEVERR_BAD_SLOT);
             continue;
         }
-        const int64_t block = slot / block_size;
-        const int64_t offset = slot - block * block_size;
-        const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * chunks + c;
-        const uint4 kv = __ldg(k + idx);
-        const uint4 vv = __ldg(v + idx);
+        const I block = static_cast<I>(slot) / block_size;
+        const I offset = static_cast<I>(slot) - block * block_size;
+        const int64_t dst =
+            ((static_cast<int64_t>(block) * num_kv_heads + h) * block_size + offset) * chunks + c;
         k_cache[dst] = kv;
         v_cache[dst] = vv;
     }
@@ -51,14 +55,22 @@ cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_ma
     const int32_t chunks = c.head_dim / 8;  // 16-byte vectors per row
     const int64_t total = static_cast<int64_t>(num_tokens) * c.num_kv_heads * chunks;
     if (total == 0) return cudaSuccess;
+    const int64_t num_slots = static_cast<int64_t>(c.num_blocks) * c.block_size;
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
     const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
-    kv_write_kernel<<<grid, threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, num_tokens,
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), c.num_kv_heads, c.block_size,
-        chunks, static_cast<int64_t>(c.num_blocks) * c.block_size, err);
-    return cudaGetLastError();
+    const bool narrow = total < (int64_t{1} << 31) && num_slots < (int64_t{1} << 31);
+    const uint4* kp = static_cast<const uint4*>(k);
+    const uint4* vp = static_cast<const uint4*>(v);
+    uint4* kc = static_cast<uint4*>(k_cache);
+    uint4* vc = static_cast<uint4*>(v_cache);
+    if (narrow)
+        return launch_pdl(kv_write_kernel<int32_t>, dim3(grid), dim3(threads), 0, stream, kp, vp,
+                          slot_mapping, num_tokens, kc, vc, c.num_kv_heads, c.block_size, chunks,
+                          num_slots, err);
+    return launch_pdl(kv_write_kernel<int64_t>, dim3(grid), dim3(threads), 0, stream, kp, vp,
+                      slot_mapping, num_tokens, kc, vc, c.num_kv_heads, c.block_size, chunks,
+                      num_slots, err);
 }
 
 }  // namespace pkv

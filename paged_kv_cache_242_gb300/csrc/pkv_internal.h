@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -13,6 +15,24 @@ constexpr int kHeadDim = 128;        // head size the attention kernels implemen
 constexpr int kConsumerWarps = 4;    // warps that compute on staged K/V tiles
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kAutoPartition = 512;  // tokens per partition in automatic split mode
+
+// Launch `kernel` on `stream` with programmatic stream serialisation allowed
+// (the kernel waits for its prerequisites itself, see pkv_device.cuh).
+template <typename... KernelArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DecodeArgs {
     const void* q;              // [S][Hq][128]
@@ -37,7 +57,14 @@ struct DecodeArgs {
     int32_t num_warps;          // stream mode: warps in the grid
 };
 
-constexpr int kStreamWarps = 8;         // warps per CTA of the streaming kernel
+#ifndef PKV_STREAM_WARPS
+#define PKV_STREAM_WARPS 8
+#endif
+#ifndef PKV_STREAM_STAGES
+#define PKV_STREAM_STAGES 3
+#endif
+constexpr int kStreamWarps = PKV_STREAM_WARPS;    // warps per CTA of the streaming kernel
+constexpr int kStreamStages = PKV_STREAM_STAGES;  // 8 KiB stages per warp
 constexpr int kStreamMaxCtas = 160;     // cap of its grid (one CTA per SM)
 constexpr int kStreamMaxSeqs = 4096;    // sequences whose prefix fits shared memory
 constexpr int kTileTokens = 16;         // tokens per streamed tile

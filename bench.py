@@ -257,7 +257,7 @@ def time_attention_only(pkv, step, dev, part, reps=200, warmup=10):
     """Average device time of one paged_decode_attention call (CUDA events)."""
     ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
                                           step.block_size, part)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev["q"].device)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev["q"].device)
     out = torch.empty_like(dev["q"])
 
     def call():
@@ -295,7 +295,7 @@ def run_pkv(args, rank, world, local_rank):
     split = part < step.max_seq_len
     ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
                                           step.block_size, args.partition_size)
-    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     out = torch.empty_like(dev["q"])
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
@@ -366,19 +366,30 @@ def run_pkv(args, rank, world, local_rank):
     # ---------------- end to end through the public API ----------------
     e2e = None
     if not args.no_e2e:
-        pin = {k: v.pin_memory() for k, v in {
-            "q": step.q, "k_new": step.k_new, "v_new": step.v_new,
-            "slot_mapping": step.slot_mapping, "block_tables": step.block_tables,
-            "seq_lens": step.seq_lens}.items()}
+        # A step's host inputs (query, new keys / values, slot mapping, block
+        # tables, lengths) staged in one pinned buffer: one host-to-device
+        # copy per step, device tensors are views of one device buffer.
+        host_inputs = {"q": step.q, "k_new": step.k_new, "v_new": step.v_new,
+                       "slot_mapping": step.slot_mapping, "block_tables": step.block_tables,
+                       "seq_lens": step.seq_lens}
+        layout, off = {}, 0
+        for k, t in host_inputs.items():
+            layout[k] = (off, t.numel() * t.element_size(), t.dtype, tuple(t.shape))
+            off = (off + layout[k][1] + 255) // 256 * 256
+        staged = torch.empty(off, dtype=torch.uint8, pin_memory=True)
+        for k, t in host_inputs.items():
+            o, n, _, _ = layout[k]
+            staged[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+        staged_dev = torch.empty(off, dtype=torch.uint8, device=device)
+        inputs = {k: staged_dev[o:o + n].view(dt).view(shape)
+                  for k, (o, n, dt, shape) in layout.items()}
         out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        h2d = off
         d2h = out_host.numel() * out_host.element_size()
-        inputs = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
         e2e_steps = max(10, min(K, 2000))
 
         def e2e_step():
-            for k in pin:
-                inputs[k].copy_(pin[k], non_blocking=True)
+            staged_dev.copy_(staged, non_blocking=True)
             pkv.kv_write(inputs["k_new"], inputs["v_new"], inputs["slot_mapping"],
                          dev["k_cache"], dev["v_cache"], err_flag=err)
             pkv.paged_decode_attention(inputs["q"], dev["k_cache"], dev["v_cache"],

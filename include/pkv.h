@@ -151,7 +151,9 @@ PKV_API size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *                 block_size); >= max_seq_len = single pass.
  *   workspace     device scratch of workspace_bytes >=
  *                 pkv_decode_workspace_bytes(...) (may be NULL when that is 0).
- *                 Its contents need no initialisation and are overwritten.
+ *                 It holds partial softmax statistics; its contents need no
+ *                 initialisation and are overwritten.  Calls that share a
+ *                 workspace must not run concurrently.
  *   out           [num_seqs][num_q_heads][head_dim], dtype of c.
  * Supported: head_dim 128, block_size 16 or 32, num_q_heads / num_kv_heads
  * <= 64, num_seqs <= 65535; other valid shapes return PKV_ERR_UNSUPPORTED.

@@ -285,8 +285,7 @@ cudaError_t launch_typed(const CUtensorMap& k_map, const CUtensorMap& v_map, con
     using G = Geometry<BS>;
     const size_t smem = 1024 + G::kRingBytes + sizeof(Control);
     auto kernel = paged_decode_kernel<T, BS, MT>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t err = ensure_smem_limit<paged_decode_kernel<T, BS, MT>>(smem);
     if (err != cudaSuccess) return err;
     dim3 grid(static_cast<unsigned>(a.max_partitions), static_cast<unsigned>(a.num_kv_heads),
               static_cast<unsigned>(a.num_seqs));

@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int S = a.num_seqs;
     const int H = a.num_kv_heads;
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&v_map);
+    }
     pdl_wait_prerequisites();
     pdl_allow_dependents();
 
@@ -206,10 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cursor_advance(iss, prefix, S, H);
     };
 
-    if (lane == 0) {
-        prefetch_tensormap(&k_map);
-        prefetch_tensormap(&v_map);
-    }
     const int prologue = count < kStages ? count : kStages;
     for (int k = 0; k < prologue; ++k) issue(k);
 
@@ -314,10 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge of the partial statistics of segments cut by warp ranges (Eq. 4):
 // out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w, M = max_w m_w.
-// One warp per (segment, query head of the group); lanes take partials 32 at
-// a time for the statistics and 4 output columns each for the weighted sum,
-// so every load of a warp is issued together.
+// One warp per (segment, query head of the group), four output columns per
+// lane.  After one round trip for the segment's position, the (m, l, acc)
+// of up to eight pieces are loaded together and folded in with the running
+// max / sum, so a segment of up to eight pieces costs two dependent memory
+// round trips.  Launched with programmatic dependent launch: its CTAs wait
+// for the streaming kernel and start as soon as it finishes.
 constexpr int kMergeWarps = 4;
+constexpr int kMergeBatch = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const DecodeArgs a) {
@@ -334,68 +338,52 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
     const int h = static_cast<int>(j - static_cast<int64_t>(s) * H);
     const int p_s = a.ws_prefix[s];
     const int nt = a.ws_prefix[s + 1] - p_s;
-    T* orow = static_cast<T*>(a.out) +
-              (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g + r) * kHeadDim;
-    uint2* ocol = reinterpret_cast<uint2*>(orow + lane * 4);  // this lane's 4 columns
-    const int col = lane * 4;
+    const int64_t total_tiles = static_cast<int64_t>(a.ws_prefix[a.num_seqs]) * H;
+    uint2* ocol = reinterpret_cast<uint2*>(
+        static_cast<T*>(a.out) +
+        (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g + r) * kHeadDim +
+        lane * 4);
     if (nt == 0) {  // empty sequence: zero output
         *ocol = make_uint2(0u, 0u);
         return;
     }
-    const int64_t total_tiles = static_cast<int64_t>(a.ws_prefix[a.num_seqs]) * H;
     const int64_t per = (total_tiles + a.num_warps - 1) / a.num_warps;
     const int64_t first = static_cast<int64_t>(p_s) * H + static_cast<int64_t>(h) * nt;
     const int64_t w0 = first / per;
     const int64_t w1 = (first + nt - 1) / per;
     if (w0 == w1) return;  // one warp covered the segment and wrote the output
     const int np = static_cast<int>(w1 - w0 + 1);
-    const size_t row0 = static_cast<size_t>(w0 + j) * g + r;  // partial p is row0 + p * g
+    const size_t row0 = static_cast<size_t>(w0 + j) * g + r;  // piece p is row row0 + p * g
 
-    // pass 1: M = max m_p and L = sum 2^(m_p - M) l_p, online over chunks of 32
     float big = -INFINITY, den = 0.f;
-    for (int base = 0; base < np; base += 32) {
-        const int p = base + lane;
-        float m = -INFINITY, l = 0.f;
-        if (p < np) {
-            m = a.ws_m[row0 + static_cast<size_t>(p) * g];
-            l = a.ws_l[row0 + static_cast<size_t>(p) * g];
-        }
-        float cm = m;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-        const float nb = fmaxf(big, cm);
-        float c = (m == -INFINITY) ? 0.f : ex2(m - nb) * l;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        den = (big == -INFINITY ? 0.f : den * ex2(big - nb)) + c;
-        big = nb;
-    }
-    if (big == -INFINITY || !(den > 0.f)) {
-        *ocol = make_uint2(0u, 0u);
-        return;
-    }
-    // pass 2: sum_p 2^(m_p - M) acc_p over this lane's four columns
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = 0; base < np; base += 32) {
-        const int p = base + lane;
-        float wt = 0.f;
-        if (p < np) {
-            const float m = a.ws_m[row0 + static_cast<size_t>(p) * g];
-            wt = m == -INFINITY ? 0.f : ex2(m - big);
+    for (int base = 0; base < np; base += kMergeBatch) {
+        float m[kMergeBatch], l[kMergeBatch];
+        float4 v[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            const size_t row = row0 + static_cast<size_t>(base + u) * g;
+            const bool live = base + u < np;
+            m[u] = live ? a.ws_m[row] : -INFINITY;
+            l[u] = live ? a.ws_l[row] : 0.f;
+            v[u] = live ? *reinterpret_cast<const float4*>(a.ws_acc + row * kHeadDim + lane * 4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const int cnt = min(32, np - base);
-#pragma unroll 4
-        for (int q = 0; q < cnt; ++q) {
-            const float wq = __shfl_sync(0xffffffffu, wt, q);
-            const float4 v = *reinterpret_cast<const float4*>(
-                a.ws_acc + (row0 + static_cast<size_t>(base + q) * g) * kHeadDim + col);
-            acc.x += wq * v.x;
-            acc.y += wq * v.y;
-            acc.z += wq * v.z;
-            acc.w += wq * v.w;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            const float nb = fmaxf(big, m[u]);
+            if (nb == -INFINITY) continue;
+            const float sa = ex2(big - nb);  // 0 while big = -inf
+            const float sb = ex2(m[u] - nb);
+            den = den * sa + l[u] * sb;
+            acc.x = acc.x * sa + v[u].x * sb;
+            acc.y = acc.y * sa + v[u].y * sb;
+            acc.z = acc.z * sa + v[u].z * sb;
+            acc.w = acc.w * sa + v[u].w * sb;
+            big = nb;
         }
     }
-    const float inv = 1.f / den;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
     *ocol = make_uint2(Mma<T>::pack(acc.x * inv, acc.y * inv), Mma<T>::pack(acc.z * inv, acc.w * inv));
 }
 
@@ -405,8 +393,7 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
     const size_t smem = 1024 + kRingBytes + sizeof(StreamControl) +
                         (2 * static_cast<size_t>(a.num_seqs) + 1) * sizeof(int32_t);
     auto kernel = paged_decode_stream_kernel<T, BS>;
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+    cudaError_t err = ensure_smem_limit<paged_decode_stream_kernel<T, BS>>(smem);
     if (err != cudaSuccess) return err;
     err = launch_pdl(kernel, dim3(ctas), dim3(kThreads), smem, stream, k_map, v_map, a);
     if (err != cudaSuccess) return err;

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "pkv.h"
@@ -32,6 +33,29 @@ cudaError_t launch_pdl(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, siz
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raise kKernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the limit reached is remembered per (kernel, device), so
+// later calls skip the driver.
+template <auto kKernel>
+cudaError_t ensure_smem_limit(size_t bytes) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<size_t> configured[kMaxDevices];
+    int device = 0;
+    cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return err;
+    if (device >= 0 && device < kMaxDevices &&
+        configured[device].load(std::memory_order_relaxed) >= bytes)
+        return cudaSuccess;
+    err = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(bytes));
+    if (err == cudaSuccess && device >= 0 && device < kMaxDevices) {
+        size_t cur = configured[device].load(std::memory_order_relaxed);
+        while (cur < bytes && !configured[device].compare_exchange_weak(cur, bytes)) {
+        }
+    }
+    return err;
 }
 
 struct DecodeArgs {

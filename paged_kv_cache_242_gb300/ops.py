@@ -97,7 +97,8 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     q [S, H_q, d]; block_tables int32 [S, max_blocks]; seq_lens int32 [S].
     ``max_seq_len`` (a host int >= every seq_len) avoids a device read; if
     omitted it is taken from ``seq_lens`` with a synchronising ``.item()``.
-    ``workspace`` (uint8 CUDA tensor) is allocated when needed and omitted.
+    ``workspace`` (uint8 CUDA tensor, zero-filled when new) is allocated
+    when needed and omitted; reuse one across calls to avoid allocations.
     """
     _check_caches(k_cache, v_cache)
     desc = cache_desc(k_cache)
@@ -121,10 +122,11 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous() and out.is_cuda,
              "out must match q")
     max_blocks = int(block_tables.shape[1])
-    need = decode_workspace_bytes(S, Hq, max_seq_len, desc.block_size, partition_size,
-                                  desc.head_dim)
-    if need > 0 and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:
+        need = decode_workspace_bytes(S, Hq, max_seq_len, desc.block_size, partition_size,
+                                      desc.head_dim)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lib = _lib.load()
     _lib.check(lib.pkv_paged_decode_attention(

@@ -252,6 +252,55 @@ def test_stream_single_long_sequence_many_partials():
     _full_step_parity(step, partition_sizes=(0,))
 
 
+def test_stream_workspace_reuse_with_leftover_contents():
+    """A workspace full of unrelated bytes, reused across shapes, gives correct outputs."""
+    a = _custom([3000, 900, 4000, 17], 32, 8, 16, "bfloat16", seed=40)
+    b = _custom([100] * 40, 16, 4, 32, "float16", seed=41)
+    need = max(pkv.decode_workspace_bytes(s.num_seqs, s.num_q_heads, s.max_seq_len, s.block_size)
+               for s in (a, b))
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8,
+                       generator=torch.Generator().manual_seed(5)).cuda()
+    for step in (a, b, a, b):
+        kc, vc = bits(step.k_cache), bits(step.v_cache)
+        ref, _, _ = oracle_step(step, kc, vc)
+        dev = to_device(step)
+        pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                     dev["v_cache"])
+        out = pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                         dev["block_tables"], dev["seq_lens"], step.num_kv_heads,
+                                         step.scale, max_seq_len=step.max_seq_len, workspace=ws)
+        assert_attention_close(out, ref, "reused workspace")
+
+
+def test_cuda_graph_replay():
+    """A captured attention call replays correctly."""
+    step = _custom([2500, 3000, 700], 32, 8, 16, "bfloat16", seed=42)
+    kc, vc = bits(step.k_cache), bits(step.v_cache)
+    ref, _, _ = oracle_step(step, kc, vc)
+    dev = to_device(step)
+    pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"], dev["v_cache"])
+    need = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
+                                      step.block_size)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(dev["q"])
+
+    def call():
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["seq_lens"], step.num_kv_heads, step.scale, out,
+                                   max_seq_len=step.max_seq_len, workspace=ws)
+
+    call()  # first call on this device before capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_attention_close(out, ref, "graph replay")
+
+
 def test_split_size_invariance():
     step = _custom([3000, 4000, 2500], 32, 8, 16, "bfloat16", seed=18)
     kc, vc = bits(step.k_cache), bits(step.v_cache)

@@ -94,16 +94,27 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_for(source: str):
-    """DRAM bytes per launch from a committed ncu capture of this exact source."""
-    path = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+TRAFFIC_SOURCES = ("decode_stream.cu", "decode_tile.cuh", "pkv_device.cuh", "pkv_internal.h")
+
+
+def kernel_source_digest() -> str:
+    """sha256 over the sources the streaming attention kernel is built from."""
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_242_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_for():
+    """DRAM bytes per launch from a committed ncu capture of these exact sources."""
+    path = os.path.join(ROOT, "profiles", "decode_stream_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    digest = hashlib.sha256(open(source, "rb").read()).hexdigest()
-    if rec.get("source_sha256") != digest:
+    if rec.get("source_sha256") != kernel_source_digest():
         return None
     return rec.get("dram_bytes_per_launch_gqa_batch")
 
@@ -440,14 +451,15 @@ def run_pkv(args, rank, world, local_rank):
         return
     hbm, kind = measured_peaks()
     achieved = a_bytes / (attn_ms * 1e-3) / 1e9
-    source = os.path.join(ROOT, "paged_kv_cache_242_gb300", "csrc", "decode_stream.cu")
     roofline = {"kernel": "paged_decode_attention (streaming kernel + merge kernel)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_kind": f"{kind} (burst copy)",
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                 "algorithmic_bytes_per_launch": a_bytes,
                 "avg_call_ms": round(attn_ms, 5),
-                "traffic": traffic_for(source)}
+                "traffic": traffic_for(),
+                "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the streaming "
+                                "kernel alone (the merge kernel reads its ~4 MB of partials from L2)"}
     cpu = None
     if world == 1 and not args.no_cpu:
         rate, _, desc, threads = oracle_sample_rate(step, 10.0)

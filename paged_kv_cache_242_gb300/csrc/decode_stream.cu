@@ -1,5 +1,5 @@
-// Streaming paged decode attention: a persistent grid with one CTA of eight
-// warps per SM, each warp an independent TMA pipeline.
+// Streaming paged decode attention: a persistent grid with one CTA of
+// kStreamWarps (7) warps per SM, each warp an independent TMA pipeline.
 //
 // What it computes is the same as the partition kernel (decode_attention.cu):
 // for every sequence and query head, softmax(scale * q K^T) V over the
@@ -18,11 +18,13 @@
 // partial (max, sum, weighted sum) statistics, which the merge kernel
 // combines by the same Eq. (4) rule.
 //
-// Pipeline.  Each warp owns kStreamStages (3) 8 KiB shared-memory stages
+// Pipeline.  Each warp owns kStreamStages (2) 8 KiB shared-memory stages
 // (K and V of one tile, two 64-column boxes each, 128-byte swizzle).  Lane 0
-// issues the TMA loads of tile k + 3 as soon as the warp has finished tile k,
-// so three tiles per warp and 24 per SM are in flight or being consumed;
-// block-table entries are fetched 32 at a time by the whole warp.  The per-tile math is
+// issues the TMA loads of tile k + 2 as soon as the warp has finished tile k,
+// so 14 tiles per SM are in flight or being consumed.  (Sweeps of warps x
+// stages on GB300 put the optimum at 7-8 warps x 2 stages: more requests in
+// flight only queue at the saturated HBM.)  Block-table entries are fetched
+// 32 at a time by the whole warp.  The per-tile math is
 // attend_block (decode_tile.cuh): mma.sync Q K^T, fp32 online softmax in the
 // log2 domain, mma.sync P V.
 //

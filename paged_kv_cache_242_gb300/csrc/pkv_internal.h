@@ -82,10 +82,10 @@ struct DecodeArgs {
 };
 
 #ifndef PKV_STREAM_WARPS
-#define PKV_STREAM_WARPS 8
+#define PKV_STREAM_WARPS 7
 #endif
 #ifndef PKV_STREAM_STAGES
-#define PKV_STREAM_STAGES 3
+#define PKV_STREAM_STAGES 2
 #endif
 constexpr int kStreamWarps = PKV_STREAM_WARPS;    // warps per CTA of the streaming kernel
 constexpr int kStreamStages = PKV_STREAM_STAGES;  // 8 KiB stages per warp

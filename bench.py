@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-extra", action="store_true", help="skip the long-context line")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also measure the tiny, OPT-13B-like and prefix-sharing workloads")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--seed", type=int, default=244)
     return ap.parse_args()
@@ -290,6 +292,92 @@ def time_attention_only(pkv, step, dev, part, reps=200, warmup=10):
     return e0.elapsed_time(e1) / reps
 
 
+def measure_attention(pkv, step, device, label, workload):
+    dev = {"q": step.q.to(device), "k_cache": step.k_cache.to(device),
+           "v_cache": step.v_cache.to(device), "block_tables": step.block_tables.to(device),
+           "seq_lens": step.seq_lens.to(device)}
+    ms = time_attention_only(pkv, step, dev, 0)
+    hbm, _ = measured_peaks()
+    gbs = attention_bytes(step) / (ms * 1e-3) / 1e9
+    del dev
+    torch.cuda.empty_cache()
+    return {"workload": workload, "attention_ms": round(ms, 4), "achieved_gbs": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / hbm, 4),
+            "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "decode_tokens_per_s": round(step.num_seqs / (ms * 1e-3), 1)}
+
+
+def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
+    """Full decode steps (copy-on-write copies + kv_write + attention) of the
+    prefix-sharing scenario, all 256 steps' inputs resident on the device."""
+    sc = W.PrefixSharingScenario(prompt_len=prompt_len, decode_steps=steps)
+    k_cache, v_cache = sc.k_cache.to(device), sc.v_cache.to(device)
+    plan = []
+    logical = unique = copies = 0
+    for _ in range(steps):
+        st = sc.next_step()
+        plan.append({k: getattr(st, k).to(device) for k in
+                     ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens", "cow_pairs")}
+                    | {"max_seq_len": st.max_seq_len, "step": st})
+        logical += attention_bytes(st)
+        unique += sc.unique_blocks_in_use() * sc.num_kv_heads * sc.block_size * sc.head_dim * 4
+        copies += int(st.cow_pairs.shape[0])
+    ws_bytes = max(pkv.decode_workspace_bytes(sc.num_seqs, sc.num_q_heads, p["max_seq_len"],
+                                              sc.block_size) for p in plan)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+    out = torch.empty_like(plan[0]["q"])
+
+    def run_all():
+        for p in plan:
+            if p["cow_pairs"].numel():
+                pkv.copy_blocks(k_cache, v_cache, p["cow_pairs"])
+            pkv.kv_write(p["k_new"], p["v_new"], p["slot_mapping"], k_cache, v_cache)
+            pkv.paged_decode_attention(p["q"], k_cache, v_cache, p["block_tables"], p["seq_lens"],
+                                       sc.num_kv_heads, p["step"].scale, out,
+                                       max_seq_len=p["max_seq_len"], workspace=ws)
+
+    run_all()  # warm-up pass (also replays the copies and writes once)
+    # restore the initial pools so the timed pass replays the same work
+    k_cache.copy_(sc.k_cache.to(device))
+    v_cache.copy_(sc.v_cache.to(device))
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    run_all()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    hbm, _ = measured_peaks()
+    return {"workload": f"16 prompts x {prompt_len} tokens x 8 samples, {steps} decode steps, "
+                        "block 32, 32 q / 8 kv heads, bf16",
+            "ms_per_step": round(ms / steps, 4),
+            "decode_tokens_per_s": round(sc.num_seqs * steps / (ms * 1e-3), 1),
+            "cow_copies": copies,
+            "logical_gbs": round(logical / (ms * 1e-3) / 1e9, 1),
+            "logical_frac_of_measured_peak": round(logical / (ms * 1e-3) / 1e9 / hbm, 4),
+            "unique_kv_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
+            "note": "logical bytes count shared prefix blocks once per sample (L2 serves the "
+                    "repeats); unique bytes count each physical block once"}
+
+
+def other_workloads(pkv, W, device, all_configs):
+    extra = {"long_context": measure_attention(
+        pkv, W.long_context(), device, "long_context",
+        "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16")}
+    if all_configs:
+        for bs in (16, 32):
+            st = W.tiny(bs)
+            extra[f"tiny_B{bs}"] = measure_attention(
+                pkv, st, device, "tiny", f"5 sequences 37/91/128/201/511, 8 heads, fp16, block {bs}")
+        extra["opt13b_like"] = measure_attention(
+            pkv, W.opt13b_like(), device, "opt13b_like",
+            "128 sequences, log-normal lengths (cap 2048), 40 heads MHA, fp16, block 16")
+        extra["prefix_sharing"] = prefix_sharing_steps(pkv, W, device, 1024)
+        extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
+    return extra
+
+
 def run_pkv(args, rank, world, local_rank):
     import paged_kv_cache_242_gb300 as pkv
     from paged_kv_cache_242_gb300 import workloads as W
@@ -426,26 +514,12 @@ def run_pkv(args, rank, world, local_rank):
                "ms_per_step": round(e2e_s * 1e3, 4), "steps": e2e_steps,
                "decode_tokens_per_s": round(world * step.num_seqs / e2e_s, 1)}
 
-    # ---------------- long-context batch: attention alone ----------------
+    # ---------------- other workloads: attention alone ----------------
     extra = {}
     if not args.no_extra and rank == 0:
         del dev, workspace
         torch.cuda.empty_cache()
-        lc = W.long_context()
-        dlc = {"q": lc.q.to(device), "k_cache": lc.k_cache.to(device),
-               "v_cache": lc.v_cache.to(device), "block_tables": lc.block_tables.to(device),
-               "seq_lens": lc.seq_lens.to(device)}
-        lc_ms = time_attention_only(pkv, lc, dlc, 0)
-        hbm, kind = measured_peaks()
-        lc_gbs = attention_bytes(lc) / (lc_ms * 1e-3) / 1e9
-        extra["long_context"] = {
-            "workload": "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16, "
-                        "512-token partitions + merge",
-            "attention_ms": round(lc_ms, 4), "achieved_gbs": round(lc_gbs, 1),
-            "frac_of_measured_peak": round(lc_gbs / hbm, 4),
-            "frac_of_nominal_8tbs": round(lc_gbs / NOMINAL_HBM_GBS, 4),
-            "decode_tokens_per_s": round(lc.num_seqs / (lc_ms * 1e-3), 1)}
-        del dlc
+        extra = other_workloads(pkv, W, device, args.all_configs)
 
     if rank != 0:
         return

@@ -373,6 +373,17 @@ def other_workloads(pkv, W, device, all_configs):
         extra["opt13b_like"] = measure_attention(
             pkv, W.opt13b_like(), device, "opt13b_like",
             "128 sequences, log-normal lengths (cap 2048), 40 heads MHA, fp16, block 16")
+        sweep = {}
+        for bs in (8, 16, 32, 64, 128):
+            st = W.gqa_batch(block_size=bs)
+            lens = st.seq_lens.to(torch.int64)
+            allocated = int(((lens + bs - 1) // bs).sum()) * bs
+            rec = measure_attention(pkv, st, device, "gqa", "GQA batch")
+            rec.pop("workload")
+            rec["position_utilisation"] = round(int(lens.sum()) / allocated, 5)
+            rec["tail_slots"] = allocated - int(lens.sum())
+            sweep[str(bs)] = rec
+        extra["block_size_sweep_gqa_batch"] = sweep
         extra["prefix_sharing"] = prefix_sharing_steps(pkv, W, device, 1024)
         extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
     return extra

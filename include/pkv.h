@@ -155,8 +155,11 @@ PKV_API size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *                 initialisation and are overwritten.  Calls that share a
  *                 workspace must not run concurrently.
  *   out           [num_seqs][num_q_heads][head_dim], dtype of c.
- * Supported: head_dim 128, block_size 16 or 32, num_q_heads / num_kv_heads
- * <= 64, num_seqs <= 65535; other valid shapes return PKV_ERR_UNSUPPORTED.
+ * Supported: head_dim 128; num_q_heads / num_kv_heads <= 64; num_seqs <=
+ * 65535; block_size 8, 16, 32, 64 or 128 in automatic mode when the group
+ * is at most 16 query heads and num_seqs <= 4096 (the streaming kernel),
+ * otherwise block_size 16 or 32 (the partition kernel).  Other valid shapes
+ * return PKV_ERR_UNSUPPORTED.
  */
 PKV_API pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -9,7 +9,8 @@
 // scores the query against one block, then the next, and combines them).
 //
 // Work split.  All (sequence, KV head) segments are cut into 16-token tiles
-// (a whole block at block size 16, half a block at 32) and laid end to end in
+// (a whole block at block size 16, a slice of one block at 32 / 64 / 128,
+// two blocks at 8) and laid end to end in
 // (sequence, head, tile) order.  Warp w of the grid takes the contiguous
 // range [w * per, (w + 1) * per) of that order, per = ceil(tiles / warps), so
 // every warp streams the same number of bytes and the grid finishes together
@@ -176,34 +177,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor iss = cursor_at(t0, prefix, S, H);
     int win_s = -1, win_base = 0, win_id = -1;
     int issued = 0;
+    // A tile is 16 token rows: rows of one block when BS >= 16, two whole
+    // blocks of 8 rows each when BS == 8 (the 128-byte swizzle repeats every
+    // 8 rows, so two 8-row boxes land exactly as one 16-row box would).
+    constexpr int kBlocksPerTile = BS < kTileTokens ? kTileTokens / BS : 1;
+    constexpr int kBoxRows = BS < kTileTokens ? BS : kTileTokens;
     auto issue = [&](int k) {
         issued = k + 1;
         const int st = k % kStages;
-        const int blk = (iss.i * kTileTokens) / BS;  // block of the sequence
-        if (iss.s != win_s || blk < win_base || blk >= win_base + 32) {
+        const int blk = (iss.i * kTileTokens) / BS;  // first block of the tile
+        const int nblocks = (lens[iss.s] + BS - 1) / BS;
+        if (iss.s != win_s || blk < win_base || blk + kBlocksPerTile > win_base + 32) {
             win_s = iss.s;
             win_base = blk;
-            const int nblocks = (lens[iss.s] + BS - 1) / BS;
             const int e = win_base + lane;
             win_id = e < nblocks ? __ldg(a.block_tables + static_cast<size_t>(iss.s) *
                                                                a.max_blocks_per_seq + e)
                                  : -1;
         }
-        const int id = __shfl_sync(0xffffffffu, win_id, blk - win_base);
+        int ids[kBlocksPerTile];
+#pragma unroll
+        for (int b = 0; b < kBlocksPerTile; ++b)
+            ids[b] = __shfl_sync(0xffffffffu, win_id, blk + b - win_base);
         if (lane == 0) {
-            const bool ok = id >= 0 && id < a.num_blocks;
+            bool ok = true;
+            int present = 0;
+#pragma unroll
+            for (int b = 0; b < kBlocksPerTile; ++b) {
+                if (blk + b < nblocks) {  // blocks past the sequence end are not read
+                    ok = ok && ids[b] >= 0 && ids[b] < a.num_blocks;
+                    ++present;
+                }
+            }
             const uint32_t full = smem_addr(&ctl->full[warp][st]);
             ctl->valid[warp][st] = ok ? 1 : 0;
             if (ok) {
                 const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
                 const uint32_t vt = kt + 2 * kHalf;
-                const int row = (iss.i * kTileTokens) % BS;
+                const int row = (iss.i * kTileTokens) % BS;  // 0 when BS <= 16
                 fence_proxy_async_shared();  // earlier generic reads of this stage
-                mbar_arrive_expect_tx(full, kStageBytes);
-                tma_load_4d(kt, &k_map, full, 0, row, iss.h, id);
-                tma_load_4d(kt + kHalf, &k_map, full, 64, row, iss.h, id);
-                tma_load_4d(vt, &v_map, full, 0, row, iss.h, id);
-                tma_load_4d(vt + kHalf, &v_map, full, 64, row, iss.h, id);
+                mbar_arrive_expect_tx(full, present * kBoxRows * 128 * 4);
+#pragma unroll
+                for (int b = 0; b < kBlocksPerTile; ++b) {
+                    if (blk + b < nblocks) {
+                        const uint32_t off = b * kBoxRows * 128;
+                        tma_load_4d(kt + off, &k_map, full, 0, row, iss.h, ids[b]);
+                        tma_load_4d(kt + kHalf + off, &k_map, full, 64, row, iss.h, ids[b]);
+                        tma_load_4d(vt + off, &v_map, full, 0, row, iss.h, ids[b]);
+                        tma_load_4d(vt + kHalf + off, &v_map, full, 64, row, iss.h, ids[b]);
+                    }
+                }
             } else {
                 report(a.err, PKV_DEVERR_BAD_BLOCK_ID);
                 mbar_arrive(full);
@@ -409,7 +432,8 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
 
 bool stream_supported(int num_seqs, int group, int block_size) {
     return num_seqs >= 1 && num_seqs <= kStreamMaxSeqs && group >= 1 && group <= 16 &&
-           (block_size == 16 || block_size == 32) &&
+           (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64 ||
+            block_size == 128) &&
            1024 + kRingBytes + sizeof(StreamControl) + (2 * static_cast<size_t>(num_seqs) + 1) * 4 <=
                232448;
 }
@@ -456,11 +480,23 @@ cudaError_t launch_paged_decode_stream(const CUtensorMap& k_map16, const CUtenso
     a.ws_l = a.ws_m + rows;
     a.ws_prefix = reinterpret_cast<int32_t*>(a.ws_l + rows);
     const bool bf16 = dtype == PKV_BF16;
-    if (block_size == 16)
-        return bf16 ? launch_stream_typed<__nv_bfloat16, 16>(k_map16, v_map16, a, (int)ctas, stream)
-                    : launch_stream_typed<__half, 16>(k_map16, v_map16, a, (int)ctas, stream);
-    return bf16 ? launch_stream_typed<__nv_bfloat16, 32>(k_map16, v_map16, a, (int)ctas, stream)
-                : launch_stream_typed<__half, 32>(k_map16, v_map16, a, (int)ctas, stream);
+    switch (block_size) {
+        case 8:
+            return bf16 ? launch_stream_typed<__nv_bfloat16, 8>(k_map16, v_map16, a, (int)ctas, stream)
+                        : launch_stream_typed<__half, 8>(k_map16, v_map16, a, (int)ctas, stream);
+        case 16:
+            return bf16 ? launch_stream_typed<__nv_bfloat16, 16>(k_map16, v_map16, a, (int)ctas, stream)
+                        : launch_stream_typed<__half, 16>(k_map16, v_map16, a, (int)ctas, stream);
+        case 32:
+            return bf16 ? launch_stream_typed<__nv_bfloat16, 32>(k_map16, v_map16, a, (int)ctas, stream)
+                        : launch_stream_typed<__half, 32>(k_map16, v_map16, a, (int)ctas, stream);
+        case 64:
+            return bf16 ? launch_stream_typed<__nv_bfloat16, 64>(k_map16, v_map16, a, (int)ctas, stream)
+                        : launch_stream_typed<__half, 64>(k_map16, v_map16, a, (int)ctas, stream);
+        default:
+            return bf16 ? launch_stream_typed<__nv_bfloat16, 128>(k_map16, v_map16, a, (int)ctas, stream)
+                        : launch_stream_typed<__half, 128>(k_map16, v_map16, a, (int)ctas, stream);
+    }
 }
 
 }  // namespace pkv

@@ -164,8 +164,10 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
     if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * c.block_size)
         return PKV_ERR_INVALID_ARG;
     if (partition_size > 0 && partition_size % c.block_size != 0) return PKV_ERR_INVALID_ARG;
-    if (c.head_dim != kHeadDim || (c.block_size != 16 && c.block_size != 32) ||
-        num_q_heads / c.num_kv_heads > 64 || num_seqs > 65535 || c.num_kv_heads > 65535)
+    const bool block_ok = c.block_size == 8 || c.block_size == 16 || c.block_size == 32 ||
+                          c.block_size == 64 || c.block_size == 128;
+    if (c.head_dim != kHeadDim || !block_ok || num_q_heads / c.num_kv_heads > 64 ||
+        num_seqs > 65535 || c.num_kv_heads > 65535)
         return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
@@ -176,6 +178,8 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
     const int32_t group = num_q_heads / c.num_kv_heads;
     const bool streaming =
         partition_size == 0 && pkv::stream_supported(num_seqs, group, c.block_size);
+    // the partition kernel stages whole blocks of 16 or 32 rows
+    if (!streaming && c.block_size != 16 && c.block_size != 32) return PKV_ERR_UNSUPPORTED;
     const int32_t part = effective_partition(max_seq_len, c.block_size, partition_size);
     const int32_t max_parts = partitions_for(max_seq_len, part);
     const size_t need = streaming ? pkv::stream_workspace_bytes(num_seqs, num_q_heads, c.num_kv_heads)
@@ -185,7 +189,9 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
     if (need > 0 && !aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
 
     CUtensorMap k_map, v_map;
-    const int box_rows = streaming ? pkv::kTileTokens : c.block_size;
+    const int box_rows =
+        streaming ? (c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens)
+                  : c.block_size;
     if (!encode_pool(&k_map, k_cache, c, box_rows) || !encode_pool(&v_map, v_cache, c, box_rows))
         return PKV_ERR_CUDA;
 

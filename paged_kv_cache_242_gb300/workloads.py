@@ -25,6 +25,10 @@ Workloads (all one decode query token per sequence, head dim 128):
                       steps; with a prompt length that is not a multiple of
                       the block size the shared partial block is copied on
                       write before each sample diverges.
+* ``BeamSearchScenario``  beams of one prompt that fork and fall out of the
+                      top-k every step, sharing blocks through refcounts.
+
+``gqa_batch`` takes a block size (8..128) for the block-size sweep.
 
 Sizes of the K/V pools are [num_blocks, H_kv, B, d]; q is [S, H_q, d]; new
 tokens are [S, H_kv, d]; slot mappings are int64; block tables and sequence
@@ -161,10 +165,11 @@ def tiny(block_size: int = 16, seed: int = 243) -> DecodeStep:
                              block_size, "float16", seed, num_blocks=64, shuffle=True)
 
 
-def gqa_batch(seed: int = 244, num_seqs: int = 64) -> DecodeStep:
+def gqa_batch(seed: int = 244, num_seqs: int = 64, block_size: int = 16) -> DecodeStep:
     g = torch.Generator().manual_seed(seed)
     context = torch.randint(512, 4097, (num_seqs,), generator=g).tolist()
-    return build_decode_step("gqa_batch", context, 32, 8, 16, "bfloat16", seed + 1000,
+    return build_decode_step("gqa_batch" if block_size == 16 else f"gqa_batch_B{block_size}",
+                             context, 32, 8, block_size, "bfloat16", seed + 1000,
                              pool_factor=1.2)
 
 
@@ -314,6 +319,90 @@ class PrefixSharingScenario:
             seq_lens=torch.from_numpy(self.manager.seq_lens_array(self.seq_ids)),
             cow_pairs=torch.tensor(pairs, dtype=torch.int64).reshape(-1, 2),
             scale=1.0 / math.sqrt(self.head_dim), meta={"step": t})
+
+
+class BeamSearchScenario:
+    """Beam search over one prompt, with blocks shared through reference counts.
+
+    Every step, each live beam appends one token (a beam whose last block
+    is still shared gets a copy first, ``cow_pairs``) and attends over its
+    sequence.  Before the next step the search keeps ``width`` beams: a
+    seeded number of beams falls out of the top-k and frees its references
+    (blocks at count zero return to the pool) and a seeded surviving beam is
+    forked into their places, sharing all of its blocks ("vLLM
+    PagedAttention & continuous batching", sharing with reference counts and
+    copy-on-write: beam search).  The kernels see only physical block ids.
+    """
+
+    def __init__(self, prompt_len: int = 100, width: int = 4, decode_steps: int = 24,
+                 block_size: int = 16, num_q_heads: int = 32, num_kv_heads: int = 8,
+                 dtype: str = "bfloat16", seed: int = 248, head_dim: int = HEAD_DIM) -> None:
+        self.width, self.decode_steps, self.block_size = width, decode_steps, block_size
+        self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
+        self.dtype, self.seed = dtype, seed
+        per_beam = -(-(prompt_len + decode_steps) // block_size)
+        self.num_blocks = width * (per_beam + 2) + 8
+        self.rng = torch.Generator().manual_seed(seed)
+        order = torch.randperm(self.num_blocks, generator=self.rng).tolist()
+        self.manager = BlockManager(self.num_blocks, block_size, free_order=order)
+        self.manager.add_sequence(0, prompt_len)
+        for b in range(1, width):
+            self.manager.fork(0, b)
+        self.live = list(range(width))
+        self.next_id = width
+        self.max_blocks = per_beam + 1
+        shape = (self.num_blocks, num_kv_heads, block_size, head_dim)
+        self.k_cache = _randn(shape, self.rng, dtype)
+        self.v_cache = _randn(shape, self.rng, dtype)
+        self.step_index = 0
+        self.total_copies = 0
+        self.savings = []  # 1 - physical / logical blocks, per step
+
+    def _prune_and_fork(self) -> None:
+        drop = int(torch.randint(0, self.width, (1,), generator=self.rng))
+        order = torch.randperm(len(self.live), generator=self.rng).tolist()
+        dropped = [self.live[i] for i in order[:drop]]
+        survivors = [s for s in self.live if s not in dropped]
+        for s in dropped:
+            self.manager.free(s)
+        best = survivors[int(torch.randint(0, len(survivors), (1,), generator=self.rng))]
+        for _ in dropped:
+            self.manager.fork(best, self.next_id)
+            survivors.append(self.next_id)
+            self.next_id += 1
+        self.live = survivors
+
+    def next_step(self) -> DecodeStep:
+        if self.step_index >= self.decode_steps:
+            raise StopIteration
+        if self.step_index > 0:
+            self._prune_and_fork()
+        slots, pairs = [], []
+        for s in self.live:
+            slot, cow = self.manager.append_slot(s)
+            slots.append(slot)
+            if cow is not None:
+                pairs.append(cow)
+        self.total_copies += len(pairs)
+        logical = sum(len(self.manager.tables[s]) for s in self.live)
+        physical = int((self.manager.refcount > 0).sum())
+        self.savings.append(1.0 - physical / logical)
+        S = len(self.live)
+        g = torch.Generator().manual_seed(self.seed * 7919 + self.step_index)
+        q = _randn((S, self.num_q_heads, self.head_dim), g, self.dtype)
+        k_new = _randn((S, self.num_kv_heads, self.head_dim), g, self.dtype)
+        v_new = _randn((S, self.num_kv_heads, self.head_dim), g, self.dtype)
+        t = self.step_index
+        self.step_index += 1
+        return DecodeStep(
+            name=f"beam_search_step{t}", dtype=self.dtype, num_q_heads=self.num_q_heads,
+            num_kv_heads=self.num_kv_heads, head_dim=self.head_dim, block_size=self.block_size,
+            q=q, k_new=k_new, v_new=v_new, slot_mapping=torch.tensor(slots, dtype=torch.int64),
+            block_tables=torch.from_numpy(
+                self.manager.block_table_array(self.live, max_blocks=self.max_blocks)),
+            seq_lens=torch.from_numpy(self.manager.seq_lens_array(self.live)),
+            cow_pairs=torch.tensor(pairs, dtype=torch.int64).reshape(-1, 2),
+            scale=1.0 / math.sqrt(self.head_dim), meta={"step": t, "live": list(self.live)})
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

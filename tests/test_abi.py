@@ -102,7 +102,9 @@ def test_host_validation_without_launch(lib):
 
     assert attn(Hq=30) == 1
     assert attn(desc=_desc(head_dim=64)) == 2
-    assert attn(desc=_desc(block_size=8), msl=32) == 2
+    assert attn(desc=_desc(block_size=24), msl=48) == 2  # not a supported block size
+    assert attn(desc=_desc(block_size=64), mb=1, part=64) == 2  # partitions need 16 or 32
+    assert attn(desc=_desc(block_size=8), mb=8) == 3  # streaming takes 8: needs a workspace
     assert attn(msl=65) == 1  # beyond 4 blocks x 16 slots
     assert attn(part=24) == 1
     assert attn(q=null) == 1

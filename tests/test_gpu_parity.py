@@ -118,6 +118,46 @@ def test_ragged_lengths_and_block_boundaries(B, dtype):
     _full_step_parity(step, partition_sizes=(0, B, 3 * B, 512, 1024))
 
 
+@pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
+def test_block_size_sweep(B):
+    """Every supported block size, lengths around block and 16-token tile edges."""
+    attended = [1, 7, 8, 9, 15, 16, 17, 31, 33, 127, 128, 129, 500, 3000]
+    step = _custom([n - 1 for n in attended], 32, 8, B, "bfloat16", seed=60 + B)
+    _full_step_parity(step, partition_sizes=(0,))
+    if B in (8, 64):
+        half = _custom([n - 1 for n in attended], 8, 8, B, "float16", seed=70 + B)
+        _full_step_parity(half, partition_sizes=(0,))
+
+
+def test_block_size_without_partition_kernel_is_unsupported():
+    step = _custom([100, 200], 32, 8, 64, "bfloat16", seed=80)
+    dev = to_device(step)
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["seq_lens"], 8, step.scale, max_seq_len=201,
+                                   partition_size=128)
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_beam_search_decode(B):
+    """Beams fork and fall out each step; copies, writes and attention match every step."""
+    sc = W.BeamSearchScenario(block_size=B)
+    kc, vc = bits(sc.k_cache), bits(sc.v_cache)
+    k_dev, v_dev = sc.k_cache.cuda(), sc.v_cache.cuda()
+    err = _err()
+    for t in range(sc.decode_steps):
+        step = sc.next_step()
+        dev = to_device(step)
+        dev["k_cache"], dev["v_cache"] = k_dev, v_dev
+        out = gpu_step(step, dev, err=err)
+        ref, kc, vc = oracle_step(step, kc, vc)
+        assert_attention_close(out, ref, f"beam search step {t}")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and sc.total_copies > 0
+    assert np.array_equal(bits(k_dev.cpu()), kc) and np.array_equal(bits(v_dev.cpu()), vc)
+
+
 @pytest.mark.parametrize("group", [1, 2, 4, 8, 16, 32, 64])
 def test_group_sizes(group):
     H_kv = 2 if group <= 16 else 1

@@ -361,6 +361,42 @@ def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
                     "repeats); unique bytes count each physical block once"}
 
 
+def swap_throughput(pkv, W, device, victims=16, reps=20):
+    """Preemption by swap: every block of `victims` sequences of the GQA batch
+    to a page-locked host pool and back, one launch per direction."""
+    st = W.gqa_batch()
+    k_dev, v_dev = st.k_cache.to(device), st.v_cache.to(device)
+    lens = st.seq_lens.to(torch.int64)
+    ids = torch.cat([st.block_tables[s, :(int(lens[s]) + st.block_size - 1) // st.block_size]
+                     for s in range(victims)]).to(torch.int64)
+    n = int(ids.numel())
+    host_k = torch.empty((n,) + tuple(st.k_cache.shape[1:]), dtype=st.k_cache.dtype).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    out_pairs = torch.stack([ids, torch.arange(n, dtype=torch.int64)], 1).to(device)
+    in_pairs = torch.stack([torch.arange(n, dtype=torch.int64), ids], 1).to(device)
+    block_bytes = st.num_kv_heads * st.block_size * st.head_dim * 2 * 2
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, args in (("out_d2h", (k_dev, v_dev, host_k, host_v, out_pairs)),
+                       ("in_h2d", (host_k, host_v, k_dev, v_dev, in_pairs))):
+        for _ in range(3):
+            pkv.swap_blocks(*args)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            pkv.swap_blocks(*args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": round(ms, 4), "gbs": round(n * block_bytes / (ms * 1e-3) / 1e9, 1)}
+    del k_dev, v_dev
+    torch.cuda.empty_cache()
+    return {"workload": f"all {n} blocks ({n * block_bytes / 1e6:.1f} MB of K+V) of {victims} "
+                        "GQA-batch sequences, device <-> page-locked host pool, one launch",
+            **res}
+
+
 def other_workloads(pkv, W, device, all_configs):
     extra = {"long_context": measure_attention(
         pkv, W.long_context(), device, "long_context",
@@ -384,6 +420,7 @@ def other_workloads(pkv, W, device, all_configs):
             rec["tail_slots"] = allocated - int(lens.sum())
             sweep[str(bs)] = rec
         extra["block_size_sweep_gqa_batch"] = sweep
+        extra["swap_gqa_batch"] = swap_throughput(pkv, W, device)
         extra["prefix_sharing"] = prefix_sharing_steps(pkv, W, device, 1024)
         extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
     return extra

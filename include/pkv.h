@@ -221,6 +221,61 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc 
                            const int64_t* src_dst_pairs, int32_t num_pairs, int32_t* err_flag,
                            void* stream);
 
+/*
+ * Copy whole blocks from one pair of pools to another: the swap path of
+ * preemption.  When physical blocks run out, all blocks of a preempted
+ * sequence are copied to CPU memory managed by a second block allocator and
+ * copied back when it resumes (vLLM PagedAttention & continuous batching,
+ * "Preemption when blocks run out", Swap).  For each pair p:
+ *     dst_k[dst_p] = src_k[src_p],  dst_v[dst_p] = src_v[src_p]
+ * over every KV head and slot, bit for bit.
+ *
+ *   src_k, src_v  source pools of src_num_blocks blocks; dst_k, dst_v
+ *                 destination pools of dst_num_blocks blocks.  Each pool is
+ *                 device memory or page-locked host memory (cudaHostAlloc,
+ *                 cudaHostRegister, torch pin_memory): the kernel reads and
+ *                 writes host pools directly over the CPU-GPU link, one launch
+ *                 for all pairs.  Pageable host memory is rejected with
+ *                 PKV_ERR_INVALID_ARG.  The two pairs of pools must not overlap.
+ *   c             shared geometry (num_kv_heads, block_size, head_dim, dtype);
+ *                 its num_blocks is not used.
+ *   src_dst_pairs DEVICE [num_pairs][2] int64 (src block, dst block).
+ *                 Destinations must be distinct.  A pair outside either pool
+ *                 is skipped and sets PKV_DEVERR_BAD_PAIR.
+ */
+PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks,
+                                   void* dst_k, void* dst_v, int32_t dst_num_blocks,
+                                   pkv_cache_desc c, const int64_t* src_dst_pairs,
+                                   int32_t num_pairs, int32_t* err_flag, void* stream);
+
+/* Most layers the *_layers calls take in one launch. */
+#define PKV_MAX_LAYERS 128
+
+/*
+ * pkv_kv_write for num_layers layers in one launch: layer l writes k[l],
+ * v[l] ([num_tokens][num_kv_heads][head_dim] each) into k_caches[l],
+ * v_caches[l] at the same slot mapping (every layer of a model shares the
+ * block tables).  k, v, k_caches, v_caches are HOST arrays of num_layers
+ * device pointers, read during the call.  1 <= num_layers <= PKV_MAX_LAYERS.
+ * Errors and conventions as pkv_kv_write.
+ */
+PKV_API pkv_status pkv_kv_write_layers(const void* const* k, const void* const* v,
+                                       const int64_t* slot_mapping, int32_t num_tokens,
+                                       void* const* k_caches, void* const* v_caches,
+                                       int32_t num_layers, pkv_cache_desc c, int32_t* err_flag,
+                                       void* stream);
+
+/*
+ * pkv_copy_blocks for num_layers layers in one launch: the same (src, dst)
+ * pairs are applied to every layer's k_caches[l], v_caches[l] (HOST arrays
+ * of num_layers device pointers).  1 <= num_layers <= PKV_MAX_LAYERS.
+ * Errors and conventions as pkv_copy_blocks.
+ */
+PKV_API pkv_status pkv_copy_blocks_layers(void* const* k_caches, void* const* v_caches,
+                                          int32_t num_layers, pkv_cache_desc c,
+                                          const int64_t* src_dst_pairs, int32_t num_pairs,
+                                          int32_t* err_flag, void* stream);
+
 /* Static, NUL-terminated name of a status code. */
 PKV_API const char* pkv_status_string(pkv_status status);
 

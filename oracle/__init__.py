@@ -61,6 +61,8 @@ def _configure(lib):
     lib.oracle_kv_write.restype = i
     lib.oracle_copy_blocks.argtypes = [u16p, u16p, i, i, i, i, i64p, i]
     lib.oracle_copy_blocks.restype = i
+    lib.oracle_transfer_blocks.argtypes = [u16p, u16p, i, u16p, u16p, i, i, i, i, i64p, i]
+    lib.oracle_transfer_blocks.restype = i
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i
     return lib
@@ -215,6 +217,21 @@ def copy_blocks(k_cache, v_cache, pairs):
     return kc, vc, status
 
 
-__all__ = ["attention", "online_attention", "partition_stats", "merge_partitions", "kv_write",
+def transfer_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """Copy whole blocks from the source pools into copies of the destination pools."""
+    lib = _load()
+    sk, sv = _bits(src_k), _bits(src_v)
+    dk, dv = _bits(dst_k).copy(), _bits(dst_v).copy()
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    snb, hkv, bs, d = _geometry(sk)
+    dnb = dk.shape[0]
+    assert dk.shape[1:] == sk.shape[1:]
+    status = lib.oracle_transfer_blocks(_ptr(sk, ctypes.c_uint16), _ptr(sv, ctypes.c_uint16), snb,
+                                        _ptr(dk, ctypes.c_uint16), _ptr(dv, ctypes.c_uint16), dnb,
+                                        hkv, bs, d, _ptr(pr, ctypes.c_int64), int(pr.shape[0]))
+    return dk, dv, status
+
+
+__all__ = ["transfer_blocks", "attention", "online_attention", "partition_stats", "merge_partitions", "kv_write",
            "copy_blocks", "f16_to_f64", "bf16_to_f64", "max_threads", "accounting", "build",
            "LIBRARY"]

@@ -402,6 +402,33 @@ int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int num_blocks, int
     return status;
 }
 
+/* ------------------------------------------------------------------ */
+/* Block transfer between two pools (swap out to, or in from, a second   */
+/* pool in host memory: vLLM PagedAttention & continuous batching,        */
+/* "Preemption when blocks run out", Swap).  For each (src, dst) pair, in */
+/* order, the whole block src of the source pools is copied to block dst  */
+/* of the destination pools.                                              */
+/* ------------------------------------------------------------------ */
+int oracle_transfer_blocks(const uint16_t *src_k, const uint16_t *src_v, int src_num_blocks,
+                           uint16_t *dst_k, uint16_t *dst_v, int dst_num_blocks,
+                           int num_kv_heads, int block_size, int head_dim, const int64_t *pairs,
+                           int num_pairs) {
+    int status = ORACLE_OK;
+    const size_t block_elems = (size_t)num_kv_heads * block_size * head_dim;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+            status = ORACLE_BAD_INDEX;
+            continue;
+        }
+        memcpy(dst_k + (size_t)dst * block_elems, src_k + (size_t)src * block_elems,
+               block_elems * sizeof(uint16_t));
+        memcpy(dst_v + (size_t)dst * block_elems, src_v + (size_t)src * block_elems,
+               block_elems * sizeof(uint16_t));
+    }
+    return status;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

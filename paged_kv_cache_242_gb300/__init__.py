@@ -8,15 +8,21 @@ behind the C ABI of ``libpkv.so`` (``include/pkv.h``), do the work:
 * ``paged_decode_attention`` exact one-query-token attention over the blocks
                              (MHA, GQA, MQA; split over long sequences with a
                              log-sum-exp merge);
-* ``copy_blocks``            whole-block copies for copy-on-write.
+* ``copy_blocks``            whole-block copies for copy-on-write;
+* ``swap_blocks``            block copies between device and page-locked host
+                             pools (preemption by swap);
+* ``kv_write_layers`` / ``copy_blocks_layers``  the same for every layer of a
+                             model in one launch.
 
 ``block_manager`` is the host-side block table / refcount manager that
 produces the kernels' inputs; ``workloads`` generates seeded synthetic
 decode batches.
 """
 from ._lib import PKVError  # noqa: F401
-from .ops import (cache_desc, copy_blocks, decode_partition_size,  # noqa: F401
-                  decode_workspace_bytes, kv_write, paged_decode_attention)
+from .ops import (cache_desc, copy_blocks, copy_blocks_layers,  # noqa: F401
+                  decode_partition_size, decode_workspace_bytes, kv_write, kv_write_layers,
+                  paged_decode_attention, swap_blocks)
 
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
-           "decode_partition_size", "cache_desc", "PKVError"]
+           "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
+           "copy_blocks_layers"]

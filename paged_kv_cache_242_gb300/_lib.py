@@ -13,6 +13,7 @@ PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 3: "PKV_ERR_WORKSPACE_TOO_SMALL", 4: "PKV_ERR_CUDA"}
 PKV_FP16, PKV_BF16 = 0, 1
+MAX_LAYERS = 128
 
 DEVERR_BAD_SLOT = 1
 DEVERR_BAD_BLOCK_ID = 2
@@ -53,6 +54,13 @@ def _declare(lib):
     lib.pkv_paged_decode_attention.restype = ctypes.c_int
     lib.pkv_copy_blocks.argtypes = [vp, vp, CacheDesc, vp, i32, i32p, vp]
     lib.pkv_copy_blocks.restype = ctypes.c_int
+    ptrs = ctypes.POINTER(ctypes.c_void_p)  # host array of device pointers
+    lib.pkv_swap_blocks.argtypes = [vp, vp, i32, vp, vp, i32, CacheDesc, vp, i32, i32p, vp]
+    lib.pkv_swap_blocks.restype = ctypes.c_int
+    lib.pkv_kv_write_layers.argtypes = [ptrs, ptrs, vp, i32, ptrs, ptrs, i32, CacheDesc, i32p, vp]
+    lib.pkv_kv_write_layers.restype = ctypes.c_int
+    lib.pkv_copy_blocks_layers.argtypes = [ptrs, ptrs, i32, CacheDesc, vp, i32, i32p, vp]
+    lib.pkv_copy_blocks_layers.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_abi_version.argtypes = []

@@ -245,4 +245,92 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc c,
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Address a kernel can use for a pool: device or managed memory as is,
+// page-locked host memory through its device mapping; null otherwise.
+static const void* device_address(const void* p) {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();  // do not leave the query's error for the next launch check
+        return nullptr;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return p;
+        case cudaMemoryTypeHost:
+            return attr.devicePointer;
+        default:
+            return nullptr;
+    }
+}
+
+pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks,
+                           void* dst_k, void* dst_v, int32_t dst_num_blocks, pkv_cache_desc c,
+                           const int64_t* src_dst_pairs, int32_t num_pairs, int32_t* err_flag,
+                           void* stream) {
+    pkv_cache_desc geometry = c;
+    geometry.num_blocks = 1;  // not used: the two pools carry their own sizes
+    pkv_status st = check_cache(geometry);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_dst_pairs || !aligned(src_dst_pairs, 8))
+        return PKV_ERR_INVALID_ARG;
+    if (pkv::block_copy_chunks(geometry) > 65535) return PKV_ERR_UNSUPPORTED;
+    const void* sk = device_address(src_k);
+    const void* sv = device_address(src_v);
+    void* dk = const_cast<void*>(device_address(dst_k));
+    void* dv = const_cast<void*>(device_address(dst_v));
+    if (!sk || !sv || !dk || !dv) return PKV_ERR_INVALID_ARG;
+    if (!aligned(sk, 16) || !aligned(sv, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+        return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::launch_transfer_blocks(sk, sv, src_num_blocks, dk, dv, dst_num_blocks,
+                                                geometry, src_dst_pairs, num_pairs, err_flag,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_kv_write_layers(const void* const* k, const void* const* v,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                               pkv_cache_desc c, int32_t* err_flag, void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0 || num_layers < 1 || num_layers > PKV_MAX_LAYERS) return PKV_ERR_INVALID_ARG;
+    if (!k || !v || !k_caches || !v_caches) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!slot_mapping || !aligned(slot_mapping, 8)) return PKV_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l) {
+        if (!k[l] || !v[l] || !k_caches[l] || !v_caches[l]) return PKV_ERR_INVALID_ARG;
+        if (!aligned(k[l], 16) || !aligned(v[l], 16) || !aligned(k_caches[l], 16) ||
+            !aligned(v_caches[l], 16))
+            return PKV_ERR_INVALID_ARG;
+    }
+    cudaError_t e = pkv::launch_kv_write_layers(k, v, slot_mapping, num_tokens, k_caches, v_caches,
+                                                num_layers, c, err_flag,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks_layers(void* const* k_caches, void* const* v_caches,
+                                  int32_t num_layers, pkv_cache_desc c,
+                                  const int64_t* src_dst_pairs, int32_t num_pairs,
+                                  int32_t* err_flag, void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0 || num_layers < 1 || num_layers > PKV_MAX_LAYERS) return PKV_ERR_INVALID_ARG;
+    if (!k_caches || !v_caches) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_dst_pairs || !aligned(src_dst_pairs, 8)) return PKV_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l) {
+        if (!k_caches[l] || !v_caches[l] || !aligned(k_caches[l], 16) || !aligned(v_caches[l], 16))
+            return PKV_ERR_INVALID_ARG;
+    }
+    if (pkv::block_copy_chunks(c) > 65535) return PKV_ERR_UNSUPPORTED;
+    cudaError_t e = pkv::launch_copy_blocks_layers(k_caches, v_caches, num_layers, c,
+                                                   src_dst_pairs, num_pairs, err_flag,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -116,4 +116,24 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_des
                                const int64_t* pairs, int32_t num_pairs, int32_t* err,
                                cudaStream_t stream);
 
+constexpr int kMaxLayers = PKV_MAX_LAYERS;
+
+// 16 KiB chunks per block of one pool (the grid's y extent for block copies).
+int64_t block_copy_chunks(const pkv_cache_desc& c);
+
+cudaError_t launch_transfer_blocks(const void* src_k, const void* src_v, int32_t src_blocks,
+                                   void* dst_k, void* dst_v, int32_t dst_blocks,
+                                   const pkv_cache_desc& c, const int64_t* pairs,
+                                   int32_t num_pairs, int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks_layers(void* const* k_caches, void* const* v_caches,
+                                      int32_t num_layers, const pkv_cache_desc& c,
+                                      const int64_t* pairs, int32_t num_pairs, int32_t* err,
+                                      cudaStream_t stream);
+
+cudaError_t launch_kv_write_layers(const void* const* k, const void* const* v,
+                                   const int64_t* slot_mapping, int32_t num_tokens,
+                                   void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                                   const pkv_cache_desc& c, int32_t* err, cudaStream_t stream);
+
 }  // namespace pkv

@@ -153,5 +153,89 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
                "pkv_copy_blocks")
 
 
+def _pairs(src_dst_pairs: torch.Tensor) -> int:
+    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.is_cuda and
+             src_dst_pairs.is_contiguous() and (src_dst_pairs.numel() == 0 or
+                                                src_dst_pairs.shape[-1] == 2),
+             "src_dst_pairs must be a contiguous CUDA int64 [num_pairs, 2] tensor")
+    return int(src_dst_pairs.numel() // 2)
+
+
+def swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                dst_v: torch.Tensor, src_dst_pairs: torch.Tensor,
+                err_flag: Optional[torch.Tensor] = None) -> None:
+    """Copy whole blocks src -> dst between two pairs of pools (preemption by swap).
+
+    Pools are CUDA tensors or page-locked host tensors (``pin_memory()``), all
+    [blocks, H_kv, B, d] of one dtype; pairs int64 [P, 2] on the device.
+    """
+    for t in (src_k, src_v, dst_k, dst_v):
+        _require(t.dim() == 4 and t.is_contiguous(), "pools must be contiguous 4-D tensors")
+        _require(t.is_cuda or t.is_pinned(), "pools must be CUDA or page-locked host tensors")
+    _require(src_k.shape == src_v.shape and dst_k.shape == dst_v.shape and
+             src_k.shape[1:] == dst_k.shape[1:] and
+             len({src_k.dtype, src_v.dtype, dst_k.dtype, dst_v.dtype}) == 1,
+             "pools must agree in heads, block size, head size and dtype")
+    desc = cache_desc(src_k)
+    P = _pairs(src_dst_pairs)
+    lib = _lib.load()
+    _lib.check(lib.pkv_swap_blocks(_ptr(src_k), _ptr(src_v), int(src_k.shape[0]), _ptr(dst_k),
+                                   _ptr(dst_v), int(dst_k.shape[0]), desc, _ptr(src_dst_pairs), P,
+                                   _err_ptr(err_flag), _stream(src_dst_pairs.device)),
+               "pkv_swap_blocks")
+
+
+def _pointer_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def _check_layers(k_caches, v_caches):
+    _require(1 <= len(k_caches) == len(v_caches) <= _lib.MAX_LAYERS,
+             f"between 1 and {_lib.MAX_LAYERS} layers, as many V caches as K caches")
+    for kc, vc in zip(k_caches, v_caches):
+        _check_caches(kc, vc)
+        _require(kc.shape == k_caches[0].shape and kc.dtype == k_caches[0].dtype,
+                 "every layer's caches must have the same shape and dtype")
+    return cache_desc(k_caches[0])
+
+
+def kv_write_layers(k, v, slot_mapping: torch.Tensor, k_caches, v_caches,
+                    err_flag: Optional[torch.Tensor] = None) -> None:
+    """kv_write for every layer in one launch: k[l], v[l] -> k_caches[l], v_caches[l]."""
+    desc = _check_layers(k_caches, v_caches)
+    _require(len(k) == len(v) == len(k_caches), "one k and v per layer")
+    T = int(slot_mapping.numel())
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and
+             slot_mapping.is_contiguous(), "slot_mapping must be a contiguous CUDA int64 tensor")
+    for kt, vt in zip(k, v):
+        _require(kt.shape == (T, desc.num_kv_heads, desc.head_dim) and vt.shape == kt.shape and
+                 kt.dtype == k_caches[0].dtype and vt.dtype == kt.dtype and kt.is_cuda and
+                 vt.is_cuda and kt.is_contiguous() and vt.is_contiguous(),
+                 "k[l], v[l] must be contiguous CUDA [num_tokens, num_kv_heads, head_dim]")
+    kp, _ka = _pointer_array(k)
+    vp, _va = _pointer_array(v)
+    kcp, _kca = _pointer_array(k_caches)
+    vcp, _vca = _pointer_array(v_caches)
+    lib = _lib.load()
+    _lib.check(lib.pkv_kv_write_layers(kp, vp, _ptr(slot_mapping), T, kcp, vcp, len(k_caches),
+                                       desc, _err_ptr(err_flag), _stream(slot_mapping.device)),
+               "pkv_kv_write_layers")
+
+
+def copy_blocks_layers(k_caches, v_caches, src_dst_pairs: torch.Tensor,
+                       err_flag: Optional[torch.Tensor] = None) -> None:
+    """copy_blocks for every layer in one launch (the same pairs in each layer)."""
+    desc = _check_layers(k_caches, v_caches)
+    P = _pairs(src_dst_pairs)
+    kcp, _kca = _pointer_array(k_caches)
+    vcp, _vca = _pointer_array(v_caches)
+    lib = _lib.load()
+    _lib.check(lib.pkv_copy_blocks_layers(kcp, vcp, len(k_caches), desc, _ptr(src_dst_pairs), P,
+                                          _err_ptr(err_flag), _stream(src_dst_pairs.device)),
+               "pkv_copy_blocks_layers")
+
+
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
-           "decode_partition_size", "cache_desc", "PKVError"]
+           "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
+           "copy_blocks_layers"]

@@ -337,4 +337,26 @@ def pin_copy_blocks_copies_whole_blocks():
     assert status != 0
 
 
+def pin_transfer_blocks_between_pools():
+    """Swap out then back in restores the bytes; only the paired blocks move."""
+    rng = np.random.default_rng(13)
+    H, d, B = 2, 4, 4
+    dev_k = rng.integers(0, 65535, (6, H, B, d), dtype=np.uint16)
+    dev_v = rng.integers(0, 65535, (6, H, B, d), dtype=np.uint16)
+    host_k = np.zeros((3, H, B, d), dtype=np.uint16)
+    host_v = np.zeros_like(host_k)
+    hk, hv, status = oracle.transfer_blocks(dev_k, dev_v, host_k, host_v, [(4, 0), (1, 2)])
+    assert status == 0
+    assert np.array_equal(hk[0], dev_k[4]) and np.array_equal(hv[2], dev_v[1])
+    assert not hk[1].any() and not hv[1].any()
+    # back in, to different device blocks
+    back_k, back_v, status = oracle.transfer_blocks(hk, hv, np.zeros_like(dev_k),
+                                                    np.zeros_like(dev_v), [(0, 5), (2, 3)])
+    assert status == 0
+    assert np.array_equal(back_k[5], dev_k[4]) and np.array_equal(back_v[3], dev_v[1])
+    assert not back_k[0].any()
+    _, _, status = oracle.transfer_blocks(dev_k, dev_v, host_k, host_v, [(0, 3)])
+    assert status != 0
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

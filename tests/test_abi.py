@@ -113,6 +113,17 @@ def test_host_validation_without_launch(lib):
     assert attn(Hq=8 * 65) == 2  # group of 65 query heads per KV head
     # split mode without a workspace
     assert attn(mb=300, msl=4097) == 3
+    # swap_blocks and the layer variants: argument checks come before any CUDA call
+    assert lib.pkv_swap_blocks(null, fake, 4, fake, fake, 4, _desc(), fake, 1, null, null) == 1
+    assert lib.pkv_swap_blocks(fake, fake, 0, fake, fake, 4, _desc(), fake, 1, null, null) == 1
+    assert lib.pkv_swap_blocks(fake, fake, 4, fake, fake, 4, _desc(), fake, 0, null, null) == 0
+    arr = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    parr = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    assert lib.pkv_kv_write_layers(parr, parr, fake, 1, parr, parr, 0, _desc(), null, null) == 1
+    assert lib.pkv_kv_write_layers(parr, parr, fake, 1, parr, parr, 129, _desc(), null, null) == 1
+    assert lib.pkv_kv_write_layers(parr, parr, fake, 0, parr, parr, 2, _desc(), null, null) == 0
+    assert lib.pkv_copy_blocks_layers(parr, parr, 2, _desc(), null, 3, null, null) == 1
+    assert lib.pkv_copy_blocks_layers(parr, parr, 2, _desc(), fake, 0, null, null) == 0
     # copy_blocks
     assert lib.pkv_copy_blocks(fake, fake, _desc(), null, 3, null, null) == 1
     assert lib.pkv_copy_blocks(null, null, _desc(), null, 0, null, null) == 0

@@ -43,6 +43,9 @@ MUTANTS = {
     "copy_blocks_direction": (
         "memmove(k_cache + (size_t)dst * block_elems, k_cache + (size_t)src * block_elems,",
         "memmove(k_cache + (size_t)src * block_elems, k_cache + (size_t)dst * block_elems,"),
+    "transfer_direction": (
+        "memcpy(dst_k + (size_t)dst * block_elems, src_k + (size_t)src * block_elems,",
+        "memcpy(dst_k + (size_t)dst * block_elems, src_k + (size_t)dst * block_elems,"),
     "empty_sequence_nonzero": ("for (size_t e = 0; e < (size_t)group * head_dim; ++e) out_group[e] = 0.0;",
                                "for (size_t e = 0; e < (size_t)group * head_dim; ++e) out_group[e] = 1.0;"),
 }

@@ -61,6 +61,9 @@ def _configure(lib):
     lib.oracle_kv_write.restype = i
     lib.oracle_copy_blocks.argtypes = [u16p, u16p, i, i, i, i, i64p, i]
     lib.oracle_copy_blocks.restype = i
+    lib.oracle_paged_prefill.argtypes = [u16p, i32p, i, i, i, u16p, u16p, i, i, i, i, i32p, i,
+                                         i32p, ctypes.c_double, f64p, i]
+    lib.oracle_paged_prefill.restype = i
     lib.oracle_transfer_blocks.argtypes = [u16p, u16p, i, u16p, u16p, i, i, i, i, i64p, i]
     lib.oracle_transfer_blocks.restype = i
     lib.oracle_max_threads.argtypes = []
@@ -217,6 +220,32 @@ def copy_blocks(k_cache, v_cache, pairs):
     return kc, vc, status
 
 
+def prefill(q, cu_q, k_cache, v_cache, block_tables, seq_lens, scale, dtype, num_threads=1):
+    """Causal fp64 attention of the last q_len tokens of each sequence.
+
+    q: [total_q, H_q, d] 16-bit patterns, sequence s's queries at rows
+    cu_q[s] .. cu_q[s+1]-1 (positions seq_len - q_len .. seq_len - 1).
+    Returns float64 [total_q, H_q, d].
+    """
+    lib = _load()
+    q = _bits(q)
+    kc, vc = _bits(k_cache), _bits(v_cache)
+    cu = np.ascontiguousarray(cu_q, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    total_q, num_q_heads, head_dim = q.shape
+    nb, hkv, bs, d = _geometry(kc)
+    num_seqs = sl.shape[0]
+    assert cu.shape[0] == num_seqs + 1 and cu[-1] == total_q and d == head_dim
+    out = np.zeros((total_q, num_q_heads, head_dim), dtype=np.float64)
+    _check(lib.oracle_paged_prefill(
+        _ptr(q, ctypes.c_uint16), _ptr(cu, ctypes.c_int32), DTYPE_CODES[dtype], num_seqs,
+        num_q_heads, _ptr(kc, ctypes.c_uint16), _ptr(vc, ctypes.c_uint16), nb, hkv, bs, d,
+        _ptr(bt, ctypes.c_int32), bt.shape[1], _ptr(sl, ctypes.c_int32), float(scale),
+        _ptr(out, ctypes.c_double), int(num_threads)), "prefill")
+    return out
+
+
 def transfer_blocks(src_k, src_v, dst_k, dst_v, pairs):
     """Copy whole blocks from the source pools into copies of the destination pools."""
     lib = _load()
@@ -232,6 +261,6 @@ def transfer_blocks(src_k, src_v, dst_k, dst_v, pairs):
     return dk, dv, status
 
 
-__all__ = ["transfer_blocks", "attention", "online_attention", "partition_stats", "merge_partitions", "kv_write",
+__all__ = ["prefill", "transfer_blocks", "attention", "online_attention", "partition_stats", "merge_partitions", "kv_write",
            "copy_blocks", "f16_to_f64", "bf16_to_f64", "max_threads", "accounting", "build",
            "LIBRARY"]

@@ -403,6 +403,93 @@ int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int num_blocks, int
 }
 
 /* ------------------------------------------------------------------ */
+/* Paged prefill attention: the prompt phase runs many query tokens of a  */
+/* sequence at once (vLLM PagedAttention & continuous batching, "Prompt  */
+/* phase, decode phase": prefill runs the known prompt as matrix-matrix  */
+/* work).  Sequence s holds n = seq_lens[s] tokens in its blocks, the    */
+/* last q_len = cu_q[s+1] - cu_q[s] of them being this call's queries,   */
+/* so query i sits at position ctx + i, ctx = n - q_len (an earlier part */
+/* of the prompt, or a shared prefix, already cached).  Causal attention: */
+/* query i attends to positions 0 .. ctx + i.  Dense two-pass softmax on  */
+/* the contiguous gathered copy, binary64.                                */
+/* q, out : [total query tokens][num_q_heads][head_dim]                   */
+/* ------------------------------------------------------------------ */
+int oracle_paged_prefill(const uint16_t *q, const int32_t *cu_q, int dtype, int num_seqs,
+                         int num_q_heads, const uint16_t *k_cache, const uint16_t *v_cache,
+                         int num_blocks, int num_kv_heads, int block_size, int head_dim,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, double scale, double *out, int num_threads) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 ||
+        head_dim <= 0 || (dtype != 0 && dtype != 1))
+        return ORACLE_BAD_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    int status = ORACLE_OK;
+    const long long pairs = (long long)num_seqs * num_kv_heads;
+    if (num_threads < 1) num_threads = 1;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+    for (long long pair = 0; pair < pairs; ++pair) {
+        const int s = (int)(pair / num_kv_heads);
+        const int h = (int)(pair % num_kv_heads);
+        const int n = seq_lens[s];
+        const int q_len = cu_q[s + 1] - cu_q[s];
+        const int ctx = n - q_len;
+        if (q_len < 0 || ctx < 0 || n > max_blocks_per_seq * block_size) {
+#pragma omp atomic write
+            status = ORACLE_BAD_INDEX;
+            continue;
+        }
+        if (q_len == 0) continue;
+        double *keys = malloc(sizeof(double) * (size_t)n * head_dim);
+        double *values = malloc(sizeof(double) * (size_t)n * head_dim);
+        double *scores = malloc(sizeof(double) * (size_t)n);
+        if (!keys || !values || !scores) {
+            free(keys); free(values); free(scores);
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+            continue;
+        }
+        const int32_t *table_row = block_tables + (size_t)s * max_blocks_per_seq;
+        int gk = gather_contiguous(k_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim,
+                                   table_row, n, h, keys);
+        int gv = gather_contiguous(v_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim,
+                                   table_row, n, h, values);
+        if (gk != ORACLE_OK || gv != ORACLE_OK) {
+            free(keys); free(values); free(scores);
+#pragma omp atomic write
+            status = ORACLE_BAD_INDEX;
+            continue;
+        }
+        for (int i = 0; i < q_len; ++i) {
+            const int visible = ctx + i + 1; /* causal: positions 0 .. ctx + i */
+            for (int j = 0; j < group; ++j) {
+                const int qh = h * group + j;
+                const size_t row = ((size_t)(cu_q[s] + i) * num_q_heads + qh) * head_dim;
+                double m = -INFINITY;
+                for (int t = 0; t < visible; ++t) {
+                    double dot = 0.0;
+                    for (int k = 0; k < head_dim; ++k)
+                        dot += widen(q[row + k], dtype) * keys[(size_t)t * head_dim + k];
+                    scores[t] = scale * dot;
+                    if (scores[t] > m) m = scores[t];
+                }
+                double denominator = 0.0;
+                double *o = out + row;
+                for (int k = 0; k < head_dim; ++k) o[k] = 0.0;
+                for (int t = 0; t < visible; ++t) {
+                    double p = exp(scores[t] - m);
+                    denominator += p;
+                    for (int k = 0; k < head_dim; ++k) o[k] += p * values[(size_t)t * head_dim + k];
+                }
+                for (int k = 0; k < head_dim; ++k) o[k] /= denominator;
+            }
+        }
+        free(keys); free(values); free(scores);
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------ */
 /* Block transfer between two pools (swap out to, or in from, a second   */
 /* pool in host memory: vLLM PagedAttention & continuous batching,        */
 /* "Preemption when blocks run out", Swap).  For each (src, dst) pair, in */

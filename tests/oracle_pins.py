@@ -359,4 +359,76 @@ def pin_transfer_blocks_between_pools():
     assert status != 0
 
 
+# ---------------------------------------------------------------------------
+# Paged prefill (causal, many query tokens per sequence)
+# ---------------------------------------------------------------------------
+def pin_prefill_hand_example():
+    """The hand example as a 3-token prompt (ctx 0), one query head per KV head.
+
+    Query 0 sees only token 0: output (7, 0).  Query 1, q = (1, 0), sees keys
+    (1,0), (0,0): scores ln2 * (1, 0), weights (2, 1) / 3, output (14/3, 7/3).
+    Query 2, q = (1, 0), sees all three: output (-2, 9).
+    """
+    for dtype in ("float16", "bfloat16"):
+        ks = [np.array([[[1, 0]], [[0, 0]], [[2, 0]]], dtype=np.float32)]
+        vs = [np.array([[[7, 0]], [[0, 7]], [[-7, 14]]], dtype=np.float32)]
+        kc, vc, bt = build_pool(ks, vs, [[5, 2]], 2, 6, dtype, fill=99.0)
+        q = to_bits([[[1, 0]], [[1, 0]], [[1, 0]]], dtype)
+        out = oracle.prefill(q, [0, 3], kc, vc, bt, [3], math.log(2.0), dtype)
+        assert np.allclose(out[0, 0], [7.0, 0.0], rtol=0, atol=1e-13), out
+        assert np.allclose(out[1, 0], [14 / 3, 7 / 3], rtol=0, atol=1e-13), out
+        assert np.allclose(out[2, 0], [-2.0, 9.0], rtol=0, atol=1e-13), out
+
+
+def pin_prefill_single_query_is_decode():
+    """One query per sequence (its last token) is exactly the decode attention."""
+    rng = np.random.default_rng(14)
+    lengths = [1, 9, 40, 77]
+    q, kc, vc, bt, lens, _ = random_case(rng, lengths, 8, 2, 16, 8, "bfloat16")
+    dec = oracle.attention(q, kc, vc, bt, lens, 0.3, "bfloat16")
+    pre = oracle.prefill(q, np.arange(len(lengths) + 1), kc, vc, bt, lens, 0.3, "bfloat16")
+    assert np.array_equal(dec, pre)
+
+
+def pin_prefill_is_causal():
+    """Changing keys and values after a query's position leaves its output unchanged."""
+    rng = np.random.default_rng(15)
+    n, q_len, H, d, B = 30, 12, 2, 8, 4
+    ks = rng.standard_normal((n, H, d)).astype(np.float32)
+    vs = rng.standard_normal((n, H, d)).astype(np.float32)
+    tables = [[int(b) for b in rng.permutation(8)]]
+    kc, vc, bt = build_pool([ks], [vs], tables, B, 8, "float16")
+    q = to_bits(rng.standard_normal((q_len, 2 * H, d)), "float16")
+    base = oracle.prefill(q, [0, q_len], kc, vc, bt, [n], 0.4, "float16")
+    ctx = n - q_len
+    for cut in (0, 5, q_len - 1):
+        ks2, vs2 = ks.copy(), vs.copy()
+        ks2[ctx + cut + 1:] = rng.standard_normal(ks2[ctx + cut + 1:].shape)
+        vs2[ctx + cut + 1:] = rng.standard_normal(vs2[ctx + cut + 1:].shape)
+        kc2, vc2, _ = build_pool([ks2], [vs2], tables, B, 8, "float16")
+        out = oracle.prefill(q, [0, q_len], kc2, vc2, bt, [n], 0.4, "float16")
+        assert np.array_equal(out[:cut + 1], base[:cut + 1])
+        if cut + 1 < q_len:
+            assert not np.array_equal(out[cut + 1:], base[cut + 1:])
+
+
+def pin_prefill_brute_force_against_library_softmax():
+    rng = np.random.default_rng(16)
+    lengths, q_lens = [5, 9], [3, 9]
+    H_q, H_kv, d, B = 4, 2, 4, 4
+    q_all, kc, vc, bt, lens, tables = random_case(rng, lengths, H_q, H_kv, d, B, "bfloat16")
+    q = to_bits(rng.standard_normal((sum(q_lens), H_q, d)), "bfloat16")
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    out = oracle.prefill(q, cu, kc, vc, bt, lens, 0.7, "bfloat16")
+    for s, (n, ql) in enumerate(zip(lengths, q_lens)):
+        for i in range(ql):
+            pos = n - ql + i
+            for qh in range(H_q):
+                h = qh // (H_q // H_kv)
+                K = np.stack([widen(kc[tables[s][t // B], h, t % B], "bfloat16") for t in range(pos + 1)])
+                V = np.stack([widen(vc[tables[s][t // B], h, t % B], "bfloat16") for t in range(pos + 1)])
+                w = softmax(0.7 * (K @ widen(q[cu[s] + i, qh], "bfloat16")))
+                assert np.allclose(out[cu[s] + i, qh], w @ V, rtol=1e-12, atol=1e-13)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

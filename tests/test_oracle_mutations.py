@@ -46,6 +46,10 @@ MUTANTS = {
     "transfer_direction": (
         "memcpy(dst_k + (size_t)dst * block_elems, src_k + (size_t)src * block_elems,",
         "memcpy(dst_k + (size_t)dst * block_elems, src_k + (size_t)dst * block_elems,"),
+    "prefill_causal_off_by_one": ("const int visible = ctx + i + 1;", "const int visible = ctx + i;"),
+    "prefill_sees_the_future": ("const int visible = ctx + i + 1;", "const int visible = n;"),
+    "prefill_query_row": ("const size_t row = ((size_t)(cu_q[s] + i) * num_q_heads + qh) * head_dim;",
+                          "const size_t row = ((size_t)(cu_q[s] + i) * num_q_heads + h) * head_dim;"),
     "empty_sequence_nonzero": ("for (size_t e = 0; e < (size_t)group * head_dim; ++e) out_group[e] = 0.0;",
                                "for (size_t e = 0; e < (size_t)group * head_dim; ++e) out_group[e] = 1.0;"),
 }

@@ -397,10 +397,59 @@ def swap_throughput(pkv, W, device, victims=16, reps=20):
             **res}
 
 
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def measure_prefill(pkv, W, device, reps=20):
+    """Causal paged prefill of the prefill batch (attention alone, after kv_write)."""
+    st = W.prefill_batch()
+    dev = {k: getattr(st, k).to(device) for k in
+           ("q", "cu_q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
+            "k_cache", "v_cache")}
+    pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"], dev["v_cache"])
+    out = torch.empty_like(dev["q"])
+
+    def call():
+        pkv.paged_prefill_attention(dev["q"], dev["cu_q"], dev["k_cache"], dev["v_cache"],
+                                    dev["block_tables"], dev["seq_lens"], st.scale, out,
+                                    max_q_len=st.max_q_len, max_seq_len=st.max_seq_len)
+
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = st.causal_flops()
+    peak, kind = measured_bf16_tflops()
+    tflops = flops / (ms * 1e-3) / 1e12
+    del dev
+    torch.cuda.empty_cache()
+    return {"workload": f"{st.num_seqs} prompts of 512..2048 tokens (total {int(st.q.shape[0])}), "
+                        "causal, 32 q / 8 kv heads, bf16, block 16",
+            "attention_ms": round(ms, 4), "useful_tflops": round(tflops, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "peak_kind": f"{kind} bf16 dense (burst)"},
+            "prompt_tokens_per_s": round(int(st.q.shape[0]) / (ms * 1e-3), 1)}
+
+
 def other_workloads(pkv, W, device, all_configs):
     extra = {"long_context": measure_attention(
         pkv, W.long_context(), device, "long_context",
-        "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16")}
+        "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16"),
+        "prefill": measure_prefill(pkv, W, device)}
     if all_configs:
         for bs in (16, 32):
             st = W.tiny(bs)

@@ -169,6 +169,43 @@ PKV_API pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache
                                       size_t workspace_bytes, void* out, int32_t* err_flag,
                                       void* stream);
 
+/*
+ * Paged prefill attention: many query tokens per sequence, causal.
+ *
+ * The prompt phase runs the known prompt as matrix-matrix work over the
+ * cache (vLLM PagedAttention & continuous batching, "Prompt phase, decode
+ * phase"); the prompt's keys and values are first written with
+ * pkv_kv_write.  Sequence s holds n = seq_lens[s] tokens in its blocks; its
+ * last q_len_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] tokens are the queries
+ * of this call, query i sitting at position n - q_len_s + i (the positions
+ * before it are an earlier chunk of the prompt or a shared prefix already
+ * cached).  Query i of query head h attends to positions 0 .. n - q_len_s + i
+ * of KV head h / (num_q_heads / num_kv_heads):
+ *     out[cu_q[s] + i][h] = softmax_t(scale * q . K_t) V_t.
+ * Products of fp16/bf16 inputs accumulate in fp32; the output is rounded to
+ * the storage dtype.
+ *
+ *   q             [total query tokens][num_q_heads][head_dim], contiguous;
+ *                 sequence s's queries are rows cu_seqlens_q[s] ..
+ *                 cu_seqlens_q[s+1] - 1.
+ *   cu_seqlens_q  DEVICE [num_seqs + 1] int32, non-decreasing, from 0.
+ *   max_q_len     HOST value >= every q_len_s (sizes the launch).
+ *   k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+ *   max_seq_len, scale: as pkv_paged_decode_attention.
+ *   out           [total query tokens][num_q_heads][head_dim].
+ * A sequence whose q_len is negative, above max_q_len or above its
+ * seq_len, or whose seq_len exceeds max_seq_len, is skipped and sets
+ * PKV_DEVERR_BAD_SEQ_LEN.  Supported: head_dim 128, block_size 8, 16, 32,
+ * 64 or 128, num_q_heads / num_kv_heads <= 64, num_seqs <= 65535.
+ */
+PKV_API pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_q,
+                                               int32_t max_q_len, const void* k_cache,
+                                               const void* v_cache, const int32_t* block_tables,
+                                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                               int32_t max_seq_len, int32_t num_seqs,
+                                               int32_t num_q_heads, pkv_cache_desc c, float scale,
+                                               void* out, int32_t* err_flag, void* stream);
+
 /* Size of the fixed device scratch of pkv_paged_decode_attention_fixed_scratch. */
 #define PKV_FIXED_SCRATCH_BYTES ((size_t)16 << 20)
 

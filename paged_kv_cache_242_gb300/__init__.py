@@ -9,6 +9,8 @@ behind the C ABI of ``libpkv.so`` (``include/pkv.h``), do the work:
                              (MHA, GQA, MQA; split over long sequences with a
                              log-sum-exp merge);
 * ``copy_blocks``            whole-block copies for copy-on-write;
+* ``paged_prefill_attention`` causal attention of many query tokens per
+                             sequence (the prompt phase) over the blocks;
 * ``swap_blocks``            block copies between device and page-locked host
                              pools (preemption by swap);
 * ``kv_write_layers`` / ``copy_blocks_layers``  the same for every layer of a
@@ -21,8 +23,8 @@ decode batches.
 from ._lib import PKVError  # noqa: F401
 from .ops import (cache_desc, copy_blocks, copy_blocks_layers,  # noqa: F401
                   decode_partition_size, decode_workspace_bytes, kv_write, kv_write_layers,
-                  paged_decode_attention, swap_blocks)
+                  paged_decode_attention, paged_prefill_attention, swap_blocks)
 
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
            "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
-           "copy_blocks_layers"]
+           "copy_blocks_layers", "paged_prefill_attention"]

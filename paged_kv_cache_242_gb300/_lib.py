@@ -54,6 +54,9 @@ def _declare(lib):
     lib.pkv_paged_decode_attention.restype = ctypes.c_int
     lib.pkv_copy_blocks.argtypes = [vp, vp, CacheDesc, vp, i32, i32p, vp]
     lib.pkv_copy_blocks.restype = ctypes.c_int
+    lib.pkv_paged_prefill_attention.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                CacheDesc, ctypes.c_float, vp, i32p, vp]
+    lib.pkv_paged_prefill_attention.restype = ctypes.c_int
     ptrs = ctypes.POINTER(ctypes.c_void_p)  # host array of device pointers
     lib.pkv_swap_blocks.argtypes = [vp, vp, i32, vp, vp, i32, CacheDesc, vp, i32, i32p, vp]
     lib.pkv_swap_blocks.restype = ctypes.c_int

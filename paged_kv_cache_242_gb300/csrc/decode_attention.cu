@@ -180,10 +180,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     for (int j = wj; j < nblk; j += kWarpsPerTile) {
         const int st = j % NST;
         const int use = j / NST;
-        if (!mbar_wait(smem_addr(&ctl->full[st]), use & 1)) {
-            report(a.err, PKV_DEVERR_TIMEOUT);
-            ctl->abort = 1;
-            break;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->full[st]), use & 1))) {
+            if (lane == 0) {
+                report(a.err, PKV_DEVERR_TIMEOUT);
+                ctl->abort = 1;
+            }
+            break;  // the whole warp stops together
         }
         if (ctl->valid[st]) {
             const uint32_t kt = smem_addr(ring + st * G::kStageBytes);

@@ -311,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             seg_from_start = true;
             reset();
         }
-        if (!mbar_wait(smem_addr(&ctl->full[warp][st]), (k / kStages) & 1)) {
-            report(a.err, PKV_DEVERR_TIMEOUT);
-            aborted = true;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->full[warp][st]), (k / kStages) & 1))) {
+            if (lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
+            aborted = true;  // the whole warp stops together
             break;
         }
         if (ctl->valid[warp][st]) {

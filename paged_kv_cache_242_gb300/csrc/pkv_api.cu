@@ -245,6 +245,59 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc c,
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_q,
+                                       int32_t max_q_len, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, int32_t max_seq_len,
+                                       int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c,
+                                       float scale, void* out, int32_t* err_flag, void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+        max_q_len < 0 || !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % c.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * c.block_size)
+        return PKV_ERR_INVALID_ARG;
+    const bool block_ok = c.block_size == 8 || c.block_size == 16 || c.block_size == 32 ||
+                          c.block_size == 64 || c.block_size == 128;
+    if (c.head_dim != kHeadDim || !block_ok || num_q_heads / c.num_kv_heads > 64 ||
+        num_seqs > 65535 || c.num_kv_heads > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
+    if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(cu_seqlens_q, 4))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t row_tiles =
+        (static_cast<int64_t>(max_q_len) * (num_q_heads / c.num_kv_heads) + 63) / 64;
+    if (row_tiles > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    CUtensorMap k_map, v_map;
+    const int box_rows = c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens;
+    if (!encode_pool(&k_map, k_cache, c, box_rows) || !encode_pool(&v_map, v_cache, c, box_rows))
+        return PKV_ERR_CUDA;
+    pkv::PrefillArgs a{};
+    a.q = q;
+    a.out = out;
+    a.cu_q = cu_seqlens_q;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.err = err_flag;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = c.num_kv_heads;
+    a.group = num_q_heads / c.num_kv_heads;
+    a.num_blocks = c.num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.max_q_len = max_q_len;
+    a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    cudaError_t e = pkv::launch_paged_prefill(k_map, v_map, a, c.dtype, c.block_size,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // Address a kernel can use for a pool: device or managed memory as is,
 // page-locked host memory through its device mapping; null otherwise.
 static const void* device_address(const void* p) {

@@ -108,6 +108,28 @@ cudaError_t launch_paged_decode(const CUtensorMap& k_map, const CUtensorMap& v_m
                                 const DecodeArgs& args, pkv_dtype dtype, int block_size,
                                 cudaStream_t stream);
 
+struct PrefillArgs {
+    const void* q;                // [total query tokens][Hq][128]
+    void* out;                    // [total query tokens][Hq][128]
+    const int32_t* cu_q;          // [S + 1] query-token offsets
+    const int32_t* block_tables;  // [S][max_blocks_per_seq]
+    const int32_t* seq_lens;      // [S] cached tokens, queries included
+    int32_t* err;                 // nullable
+    int32_t max_blocks_per_seq;
+    int32_t num_seqs;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t group;
+    int32_t num_blocks;
+    int32_t max_seq_len;
+    int32_t max_q_len;
+    float scale_log2;
+};
+
+cudaError_t launch_paged_prefill(const CUtensorMap& k_map16, const CUtensorMap& v_map16,
+                                 const PrefillArgs& args, pkv_dtype dtype, int block_size,
+                                 cudaStream_t stream);
+
 cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
                             int32_t num_tokens, void* k_cache, void* v_cache,
                             const pkv_cache_desc& c, int32_t* err, cudaStream_t stream);

@@ -137,6 +137,51 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def paged_prefill_attention(q: torch.Tensor, cu_seqlens_q: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            seq_lens: torch.Tensor, scale: Optional[float] = None,
+                            out: Optional[torch.Tensor] = None, *, max_q_len: Optional[int] = None,
+                            max_seq_len: Optional[int] = None,
+                            err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Causal attention of the last q_len cached tokens of each sequence.
+
+    q [total_q, H_q, d]; cu_seqlens_q int32 [S + 1] (sequence s's queries are
+    rows cu[s]..cu[s+1]-1 and sit at its last q_len positions); seq_lens int32
+    [S] counts every cached token including the queries.  ``max_q_len`` and
+    ``max_seq_len`` (host ints) avoid device reads when given.
+    """
+    _check_caches(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    _require(q.dim() == 3 and q.shape[2] == desc.head_dim and q.dtype == k_cache.dtype and
+             q.is_cuda and q.is_contiguous(), "q must be a contiguous CUDA [total_q, H_q, d] tensor")
+    S = int(seq_lens.numel())
+    _require(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.numel() == S + 1 and
+             cu_seqlens_q.is_cuda and cu_seqlens_q.is_contiguous(),
+             "cu_seqlens_q must be a contiguous CUDA int32 [num_seqs + 1] tensor")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+             block_tables.shape[0] == S and block_tables.is_contiguous() and block_tables.is_cuda,
+             "block_tables must be a contiguous CUDA int32 [num_seqs, max_blocks] tensor")
+    _require(seq_lens.dtype == torch.int32 and seq_lens.is_cuda and seq_lens.is_contiguous(),
+             "seq_lens must be a contiguous CUDA int32 [num_seqs] tensor")
+    if scale is None:
+        scale = desc.head_dim ** -0.5
+    if max_q_len is None:
+        max_q_len = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if S > 0 else 0
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if S > 0 else 0
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous() and out.is_cuda,
+             "out must match q")
+    lib = _lib.load()
+    _lib.check(lib.pkv_paged_prefill_attention(
+        _ptr(q), _ptr(cu_seqlens_q), int(max_q_len), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(seq_lens), int(max_seq_len), S,
+        int(q.shape[1]), desc, ctypes.c_float(float(scale)), _ptr(out), _err_ptr(err_flag),
+        _stream(q.device)), "pkv_paged_prefill_attention")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor,
                 err_flag: Optional[torch.Tensor] = None) -> None:
     """Copy whole blocks src -> dst of both caches; pairs int64 [P, 2] on the device."""
@@ -238,4 +283,4 @@ def copy_blocks_layers(k_caches, v_caches, src_dst_pairs: torch.Tensor,
 
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
            "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
-           "copy_blocks_layers"]
+           "copy_blocks_layers", "paged_prefill_attention"]

@@ -27,6 +27,8 @@ Workloads (all one decode query token per sequence, head dim 128):
                       write before each sample diverges.
 * ``BeamSearchScenario``  beams of one prompt that fork and fall out of the
                       top-k every step, sharing blocks through refcounts.
+* ``prefill_batch`` / ``build_prefill_step``  prompts (optionally after a
+                      cached context) for causal paged prefill attention.
 
 ``gqa_batch`` takes a block size (8..128) for the block-size sweep.
 
@@ -319,6 +321,98 @@ class PrefixSharingScenario:
             seq_lens=torch.from_numpy(self.manager.seq_lens_array(self.seq_ids)),
             cow_pairs=torch.tensor(pairs, dtype=torch.int64).reshape(-1, 2),
             scale=1.0 / math.sqrt(self.head_dim), meta={"step": t})
+
+
+@dataclass
+class PrefillStep:
+    """Inputs of one prefill call: the prompt tokens' kv_write, then causal attention."""
+    name: str
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    q: torch.Tensor             # [total_q, H_q, d]
+    cu_q: torch.Tensor          # int32 [S + 1]
+    k_new: torch.Tensor         # [total_q, H_kv, d] keys of the prompt tokens
+    v_new: torch.Tensor
+    slot_mapping: torch.Tensor  # int64 [total_q]
+    block_tables: torch.Tensor
+    seq_lens: torch.Tensor      # cached context + prompt tokens
+    scale: float
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    meta: Dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.numel())
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max().item()) if self.seq_lens.numel() else 0
+
+    @property
+    def max_q_len(self) -> int:
+        return int((self.cu_q[1:] - self.cu_q[:-1]).max().item()) if self.seq_lens.numel() else 0
+
+    def causal_flops(self) -> int:
+        """Useful flops: 4 * head_dim per (query head, visible key)."""
+        total = 0
+        for s in range(self.num_seqs):
+            ql = int(self.cu_q[s + 1] - self.cu_q[s])
+            ctx = int(self.seq_lens[s]) - ql
+            total += ql * ctx + ql * (ql + 1) // 2
+        return total * 4 * self.head_dim * self.num_q_heads
+
+
+def build_prefill_step(name: str, ctx_lens: Sequence[int], q_lens: Sequence[int],
+                       num_q_heads: int, num_kv_heads: int, block_size: int, dtype: str,
+                       seed: int, pool_factor: float = 1.2,
+                       head_dim: int = HEAD_DIM) -> PrefillStep:
+    """Sequences with ``ctx_lens`` tokens already cached get ``q_lens`` prompt
+    tokens: their slots come from the block manager (new blocks as the last
+    fills), their keys / values are written with kv_write, and the prompt's
+    queries attend causally over the context and the prompt so far."""
+    g = torch.Generator().manual_seed(int(seed))
+    ctx = [int(c) for c in ctx_lens]
+    ql = [int(x) for x in q_lens]
+    needed = sum(-(-(c + x) // block_size) for c, x in zip(ctx, ql))
+    num_blocks = max(1, math.ceil(pool_factor * needed))
+    order = torch.randperm(num_blocks, generator=g).tolist()
+    manager = BlockManager(num_blocks, block_size, free_order=order)
+    slots: List[int] = []
+    for s, (c, x) in enumerate(zip(ctx, ql)):
+        manager.add_sequence(s, c)
+        for _ in range(x):
+            slots.append(manager.append_slot(s)[0])
+    shape = (num_blocks, num_kv_heads, block_size, head_dim)
+    k_cache = _randn(shape, g, dtype)
+    v_cache = _randn(shape, g, dtype)
+    total = sum(ql)
+    q = _randn((total, num_q_heads, head_dim), g, dtype)
+    k_new = _randn((total, num_kv_heads, head_dim), g, dtype)
+    v_new = _randn((total, num_kv_heads, head_dim), g, dtype)
+    seq_ids = list(range(len(ctx)))
+    cu = [0]
+    for x in ql:
+        cu.append(cu[-1] + x)
+    return PrefillStep(
+        name=name, dtype=dtype, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=block_size, q=q, cu_q=torch.tensor(cu, dtype=torch.int32),
+        k_new=k_new, v_new=v_new, slot_mapping=torch.tensor(slots, dtype=torch.int64),
+        block_tables=torch.from_numpy(manager.block_table_array(seq_ids)),
+        seq_lens=torch.from_numpy(manager.seq_lens_array(seq_ids)),
+        scale=1.0 / math.sqrt(head_dim), k_cache=k_cache, v_cache=v_cache,
+        meta={"seed": int(seed), "num_blocks": num_blocks})
+
+
+def prefill_batch(seed: int = 249, num_seqs: int = 16) -> PrefillStep:
+    """Prompts of 512..2048 tokens from an empty cache, 32 / 8 heads, bf16, block 16."""
+    g = torch.Generator().manual_seed(seed)
+    q_lens = torch.randint(512, 2049, (num_seqs,), generator=g).tolist()
+    return build_prefill_step("prefill_batch", [0] * num_seqs, q_lens, 32, 8, 16, "bfloat16",
+                              seed + 1000)
 
 
 class BeamSearchScenario:

@@ -124,6 +124,22 @@ def test_host_validation_without_launch(lib):
     assert lib.pkv_kv_write_layers(parr, parr, fake, 0, parr, parr, 2, _desc(), null, null) == 0
     assert lib.pkv_copy_blocks_layers(parr, parr, 2, _desc(), null, 3, null, null) == 1
     assert lib.pkv_copy_blocks_layers(parr, parr, 2, _desc(), fake, 0, null, null) == 0
+    # prefill
+    def prefill(**kw):
+        a = dict(q=fake, cu=fake, mq=4, kc=fake, vc=fake, bt=fake, mb=4, sl=fake, msl=64, S=2,
+                 Hq=32, desc=_desc(), scale=0.1, out=fake)
+        a.update(kw)
+        return lib.pkv_paged_prefill_attention(a["q"], a["cu"], a["mq"], a["kc"], a["vc"], a["bt"],
+                                               a["mb"], a["sl"], a["msl"], a["S"], a["Hq"],
+                                               a["desc"], ctypes.c_float(a["scale"]), a["out"],
+                                               null, null)
+    assert prefill(cu=null) == 1
+    assert prefill(Hq=30) == 1
+    assert prefill(mq=-1) == 1
+    assert prefill(msl=65) == 1
+    assert prefill(desc=_desc(head_dim=64)) == 2
+    assert prefill(desc=_desc(block_size=24), msl=48) == 2
+    assert prefill(S=0) == 0 and prefill(mq=0) == 0
     # copy_blocks
     assert lib.pkv_copy_blocks(fake, fake, _desc(), null, 3, null, null) == 1
     assert lib.pkv_copy_blocks(null, null, _desc(), null, 0, null, null) == 0

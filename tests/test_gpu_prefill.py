@@ -1,0 +1,97 @@
+"""Paged prefill attention on the GPU against the fp64 oracle."""
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_242_gb300 as pkv
+from paged_kv_cache_242_gb300 import _lib
+from paged_kv_cache_242_gb300 import workloads as W
+from paged_kv_cache_242_gb300.workloads import bits
+
+from gpu_helpers import THREADS, assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _lib.load()
+
+
+def _run(step, err=None):
+    dev = {k: getattr(step, k).cuda() for k in
+           ("q", "cu_q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
+            "k_cache", "v_cache")}
+    pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"], dev["v_cache"],
+                 err_flag=err)
+    out = pkv.paged_prefill_attention(dev["q"], dev["cu_q"], dev["k_cache"], dev["v_cache"],
+                                      dev["block_tables"], dev["seq_lens"], step.scale,
+                                      max_q_len=step.max_q_len, max_seq_len=step.max_seq_len,
+                                      err_flag=err)
+    return out, dev
+
+
+def _reference(step):
+    kc, vc, status = oracle.kv_write(bits(step.k_new), bits(step.v_new), step.slot_mapping.numpy(),
+                                     bits(step.k_cache), bits(step.v_cache))
+    assert status == 0
+    return oracle.prefill(bits(step.q), step.cu_q.numpy(), kc, vc, step.block_tables.numpy(),
+                          step.seq_lens.numpy(), step.scale, step.dtype, num_threads=THREADS)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32, 128])
+@pytest.mark.parametrize("heads", [(8, 8), (32, 8), (16, 2)])
+def test_prefill_ragged(B, heads):
+    """Contexts and prompt lengths around 16-token sub-tiles and 64-key tiles."""
+    H_q, H_kv = heads
+    ctx = [0, 5, 16, 100, 0, 37]
+    ql = [1, 7, 16, 65, 200, 64]
+    step = W.build_prefill_step("ragged", ctx, ql, H_q, H_kv, B, "bfloat16", seed=100 + B + H_q)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(step, err)
+    ref = _reference(step)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, f"prefill B={B} heads={heads}")
+
+
+def test_prefill_fp16_and_mqa():
+    step = W.build_prefill_step("fp16", [300, 0], [129, 255], 8, 1, 16, "float16", seed=7)
+    out, _ = _run(step)
+    assert_attention_close(out, _reference(step), "prefill fp16 MQA")
+
+
+def test_prefill_larger_batch():
+    step = W.build_prefill_step("larger", [512, 0, 1000, 64], [512, 700, 300, 1024], 32, 8, 16,
+                                "bfloat16", seed=8)
+    out, _ = _run(step)
+    assert_attention_close(out, _reference(step), "prefill larger")
+
+
+def test_prefill_single_query_equals_decode():
+    """One query per sequence: prefill and decode attention agree with the oracle."""
+    step = W.build_prefill_step("one", [10, 400, 3000], [1, 1, 1], 32, 8, 16, "bfloat16", seed=9)
+    out, dev = _run(step)
+    dec = pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                     dev["seq_lens"], 8, step.scale, max_seq_len=step.max_seq_len)
+    torch.cuda.synchronize()
+    ref = _reference(step)
+    assert_attention_close(out, ref, "prefill q_len 1")
+    assert_attention_close(dec, ref, "decode")
+
+
+def test_prefill_bad_lengths_set_flag():
+    step = W.build_prefill_step("bad", [10, 10], [5, 5], 8, 8, 16, "bfloat16", seed=10)
+    dev = {k: getattr(step, k).cuda() for k in
+           ("q", "cu_q", "block_tables", "seq_lens", "k_cache", "v_cache")}
+    dev["seq_lens"][1] = 3  # fewer cached tokens than queries
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(dev["q"])
+    pkv.paged_prefill_attention(dev["q"], dev["cu_q"], dev["k_cache"], dev["v_cache"],
+                                dev["block_tables"], dev["seq_lens"], step.scale, out,
+                                max_q_len=5, max_seq_len=15, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & _lib.DEVERR_BAD_SEQ_LEN
+    assert torch.isfinite(out.float()).all()

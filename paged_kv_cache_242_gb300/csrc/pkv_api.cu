@@ -271,7 +271,7 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
         !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(cu_seqlens_q, 4))
         return PKV_ERR_INVALID_ARG;
     const int64_t row_tiles =
-        (static_cast<int64_t>(max_q_len) * (num_q_heads / c.num_kv_heads) + 63) / 64;
+        (static_cast<int64_t>(max_q_len) * (num_q_heads / c.num_kv_heads) + 15) / 16;
     if (row_tiles > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     CUtensorMap k_map, v_map;
     const int box_rows = c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens;

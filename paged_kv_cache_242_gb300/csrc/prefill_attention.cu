@@ -11,27 +11,30 @@
 // tile with the running max / running sum of Eq. (4) of "Serving Language
 // Models Within a Memory Budget".
 //
-// Work decomposition.  One CTA per (64-row tile, KV head, sequence), where
+// Work decomposition.  One CTA per (128-row tile, KV head, sequence), where
 // a row is one (query token, query head of the KV head's group) pair, so
 // the group shares every K/V tile.  Row tiles run longest-first (the last
-// rows see the most keys).  Warp 4 is a TMA producer: it streams 64-key
+// rows see the most keys).  Warp 8 is a TMA producer: it streams 64-key
 // tiles of K and V (16-row boxes of the 4-D pool view, 128-byte swizzle,
 // two 8-row boxes per 16 keys at block size 8) into a three-stage ring
-// guarded by full / empty mbarriers.  Warps 0-3 own 16 rows each and
+// guarded by full / empty mbarriers.  Warps 0-7 own 16 rows each and
 // consume every tile: S = Q K^T with mma.sync m16n8k16 (Q fragments held in
 // registers), per-row causal mask, fp32 online softmax in the log2 domain,
 // O += P V with P split into high and low 16-bit parts.  Each row's output
 // is O / l, rounded to the storage type.
 //
-// The contraction is dense here: 64 rows x 64 keys x 128 per tile and
-// direction, ~64 flops per K/V byte read at 4 query heads per KV head.
+// The contraction is dense here: 128 rows x 64 keys x 128 per tile and
+// direction, ~128 flops per K/V byte read at 4 query heads per KV head.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;                      // consumer warps, 16 rows each
+#ifndef PKV_PREFILL_WARPS
+#define PKV_PREFILL_WARPS 8
+#endif
+constexpr int kWarps = PKV_PREFILL_WARPS;      // consumer warps, 16 rows each
 constexpr int kThreads = (kWarps + 1) * 32;    // + the TMA producer warp
 constexpr int kRows = kWarps * 16;             // rows per CTA
 constexpr int kKeys = 64;                      // keys per stage

@@ -16,6 +16,10 @@ Contents
 * ``partition_stats`` / ``merge_partitions``  per-partition (m, l, acc)
                            statistics and their Eq. (4) merge.
 * ``kv_write`` / ``copy_blocks``  byte-exact slot scatter and block copy.
+* ``e4m3_to_f64`` / ``e4m3_from_f32`` / ``kv_write_fp8`` / ``attention_fp8``
+                           the 8-bit cache variant: E4M3 codes with one
+                           scale per pool (stored E4M3(x / scale), read
+                           back as code * scale).
 * ``accounting``           the pages' byte / block / waste / utilisation
                            formulas (pure Python).
 
@@ -66,6 +70,17 @@ def _configure(lib):
     lib.oracle_paged_prefill.restype = i
     lib.oracle_transfer_blocks.argtypes = [u16p, u16p, i, u16p, u16p, i, i, i, i, i64p, i]
     lib.oracle_transfer_blocks.restype = i
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    f32 = ctypes.c_float
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+    lib.oracle_e4m3_from_f32.argtypes = [f32]
+    lib.oracle_e4m3_from_f32.restype = ctypes.c_uint8
+    lib.oracle_kv_write_fp8.argtypes = [u16p, u16p, i, i64p, i, u8p, u8p, i, i, i, i, f32, f32]
+    lib.oracle_kv_write_fp8.restype = i
+    lib.oracle_paged_attention_fp8.argtypes = [u16p, i, i, i, u8p, u8p, i, i, i, i, i32p, i, i32p,
+                                               ctypes.c_double, f32, f32, f64p, i]
+    lib.oracle_paged_attention_fp8.restype = i
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i
     return lib
@@ -106,6 +121,62 @@ def f16_to_f64(bits: int) -> float:
 
 def bf16_to_f64(bits: int) -> float:
     return _load().oracle_bf16_to_f64(bits)
+
+
+def e4m3_to_f64(code: int) -> float:
+    """Exact value of one E4M3 code (NaN for 0x7f / 0xff)."""
+    return _load().oracle_e4m3_to_f64(int(code) & 0xFF)
+
+
+def e4m3_from_f32(x: float) -> int:
+    """Nearest E4M3 code of a binary32 value (ties to even, saturating at 448)."""
+    return int(_load().oracle_e4m3_from_f32(float(np.float32(x))))
+
+
+def _codes(array: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(array)
+    if a.dtype.itemsize != 1:
+        raise TypeError(f"expected 8-bit codes, got {a.dtype}")
+    return a.view(np.uint8)
+
+
+def kv_write_fp8(k, v, dtype, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    """Quantising slot scatter into copies of E4M3 pools; returns (kc, vc, status)."""
+    lib = _load()
+    k, v = _bits(k), _bits(v)
+    kc, vc = _codes(k_cache).copy(), _codes(v_cache).copy()
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    nb, hkv, bs, d = _geometry(kc)
+    status = lib.oracle_kv_write_fp8(
+        _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16), DTYPE_CODES[dtype],
+        _ptr(sm, ctypes.c_int64), int(sm.shape[0]), _ptr(kc, ctypes.c_uint8),
+        _ptr(vc, ctypes.c_uint8), nb, hkv, bs, d, float(k_scale), float(v_scale))
+    return kc, vc, status
+
+
+def attention_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v_scale, dtype,
+                  num_threads=1):
+    """Dense fp64 attention over E4M3 pools read back as code * scale.
+
+    q: [S, H_q, d] 16-bit patterns of ``dtype``; k_cache, v_cache: [NB, H_kv, B, d]
+    uint8 codes.  Returns float64 [S, H_q, d].
+    """
+    lib = _load()
+    q = _bits(q)
+    kc, vc = _codes(k_cache), _codes(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    num_seqs, num_q_heads, head_dim = q.shape
+    nb, hkv, bs, d = _geometry(kc)
+    assert d == head_dim and vc.shape == kc.shape and bt.shape[0] == num_seqs
+    out = np.zeros((num_seqs, num_q_heads, head_dim), dtype=np.float64)
+    _check(lib.oracle_paged_attention_fp8(
+        _ptr(q, ctypes.c_uint16), DTYPE_CODES[dtype], num_seqs, num_q_heads,
+        _ptr(kc, ctypes.c_uint8), _ptr(vc, ctypes.c_uint8), nb, hkv, bs, d,
+        _ptr(bt, ctypes.c_int32), bt.shape[1], _ptr(sl, ctypes.c_int32), float(scale),
+        float(k_scale), float(v_scale), _ptr(out, ctypes.c_double), int(num_threads)),
+        "attention_fp8")
+    return out
 
 
 def _geometry(k_cache):
@@ -261,6 +332,7 @@ def transfer_blocks(src_k, src_v, dst_k, dst_v, pairs):
     return dk, dv, status
 
 
-__all__ = ["prefill", "transfer_blocks", "attention", "online_attention", "partition_stats", "merge_partitions", "kv_write",
+__all__ = ["prefill", "transfer_blocks", "e4m3_to_f64", "e4m3_from_f32", "kv_write_fp8",
+           "attention_fp8", "attention", "online_attention", "partition_stats", "merge_partitions", "kv_write",
            "copy_blocks", "f16_to_f64", "bf16_to_f64", "max_threads", "accounting", "build",
            "LIBRARY"]

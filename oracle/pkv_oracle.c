@@ -19,7 +19,9 @@
  * so the row of token slot `o` of physical block `b`, KV head `h`, starts at
  *     ((b * num_kv_heads + h) * block_size + o) * head_dim.
  * Scalars are stored as IEEE binary16 (dtype 0) or bfloat16 (dtype 1) bit
- * patterns and are widened to binary64 exactly before any arithmetic.
+ * patterns and are widened to binary64 exactly before any arithmetic.  The
+ * 8-bit cache variant stores one-byte E4M3 codes with one scale factor per
+ * pool (see the FP8 section below).
  */
 #include <math.h>
 #include <stdint.h>
@@ -69,6 +71,56 @@ static double widen(uint16_t bits, int dtype) {
 }
 
 /* ------------------------------------------------------------------ */
+/* FP8 E4M3 (the OCP 8-bit floating-point E4M3 encoding): 1 sign bit, 4  */
+/* exponent bits with bias 7, 3 mantissa bits, no infinities; exponent   */
+/* 15 with mantissa 7 is NaN, so the largest finite magnitude is         */
+/* 1.75 * 2^8 = 448.  Exponent 0 holds the subnormals mantissa * 2^-9.   */
+/* The pages say only that changing the key-value precision changes the  */
+/* numerics ("Serving Language Models Within a Memory Budget", section 4); */
+/* the reading used here: a pool stores code = E4M3(x / scale), rounded   */
+/* from the binary32 quotient, and reads back code * scale.               */
+/* ------------------------------------------------------------------ */
+double oracle_e4m3_to_f64(uint8_t code) {
+    int sign = code >> 7;
+    int exponent = (code >> 3) & 0xf;
+    int mantissa = code & 7;
+    double magnitude;
+    if (exponent == 15 && mantissa == 7) {
+        magnitude = NAN;
+    } else if (exponent == 0) {
+        magnitude = ldexp((double)mantissa, -9);
+    } else {
+        magnitude = ldexp((double)(8 + mantissa), exponent - 10);
+    }
+    return sign ? -magnitude : magnitude;
+}
+
+/* Nearest E4M3 code of a binary32 value, ties to the even code.  In the
+ * binade [2^e, 2^(e+1)), e >= -6, neighbouring values are 2^(e-3) apart;
+ * below 2^-6 (the subnormals) they are 2^-9 apart, the spacing of e = -6.
+ * With steps = |x| / spacing rounded to an integer r, the code is
+ * (e + 7) * 8 + (r - 8): r = 16 carries into the next binade and r < 8
+ * gives the subnormal codes.  Magnitudes of 448 and above, infinities
+ * included, saturate to 448; NaN gives 0x7f. */
+uint8_t oracle_e4m3_from_f32(float x) {
+    if (isnan(x)) return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7e;
+    int e = -6;
+    if (a >= ldexp(1.0, -6)) {
+        int exponent;
+        frexp(a, &exponent); /* a = f * 2^exponent, f in [0.5, 1) */
+        e = exponent - 1;
+    }
+    const double steps = a / ldexp(1.0, e - 3); /* exact: division by a power of two */
+    double r = floor(steps);
+    const double remainder = steps - r;
+    if (remainder > 0.5 || (remainder == 0.5 && fmod(r, 2.0) == 1.0)) r += 1.0;
+    return (uint8_t)(sign | ((e + 7) * 8 + ((int)r - 8)));
+}
+
+/* ------------------------------------------------------------------ */
 /* Gather: logical token t of sequence s lives in physical block         */
 /* block_tables[s][t / B], slot t % B (vLLM PagedAttention & continuous  */
 /* batching, "PagedAttention: fixed blocks, non-contiguous physical      */
@@ -93,6 +145,23 @@ static int gather_contiguous(const uint16_t *cache, int dtype, int num_blocks, i
     return ORACLE_OK;
 }
 
+/* The same gather from a pool of E4M3 codes: each value is read back as
+ * code * factor (the pool's scale), exactly, in binary64. */
+static int gather_contiguous_e4m3(const uint8_t *cache, double factor, int num_blocks,
+                                  int num_kv_heads, int block_size, int head_dim,
+                                  const int32_t *table_row, int n, int h, double *dst) {
+    for (int t = 0; t < n; ++t) {
+        int32_t physical = table_row[t / block_size];
+        int slot = t % block_size;
+        if (physical < 0 || physical >= num_blocks) return ORACLE_BAD_INDEX;
+        const uint8_t *row =
+            cache + (((size_t)physical * num_kv_heads + h) * block_size + slot) * head_dim;
+        for (int k = 0; k < head_dim; ++k)
+            dst[(size_t)t * head_dim + k] = factor * oracle_e4m3_to_f64(row[k]);
+    }
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* Dense attention on the contiguous copy, two passes, binary64.         */
 /* PagedAttention keeps the attention maths unchanged and only changes    */
@@ -106,10 +175,42 @@ static int gather_contiguous(const uint16_t *cache, int dtype, int num_blocks, i
 /* Inference section 1; contiguous groups is the plainest mapping).       */
 /* An empty sequence (n = 0) yields a zero output row.                    */
 /* ------------------------------------------------------------------ */
-int oracle_paged_attention(const uint16_t *q, int dtype, int num_seqs, int num_q_heads,
-                           const uint16_t *k_cache, const uint16_t *v_cache, int num_blocks,
-                           int num_kv_heads, int block_size, int head_dim,
-                           const int32_t *block_tables, int max_blocks_per_seq,
+/* Two-pass dense softmax of the `group` query heads of KV head h of
+ * sequence s over its n gathered key / value rows. */
+static void attend_group(const uint16_t *q, int dtype, int s, int h, int group, int num_q_heads,
+                         int head_dim, int n, const double *keys, const double *values,
+                         double *scores, double scale, double *out_group) {
+    for (int i = 0; i < group; ++i) {
+        const int qh = h * group + i;
+        const uint16_t *q_row = q + ((size_t)s * num_q_heads + qh) * head_dim;
+        /* pass 1: scaled scores and their maximum */
+        double m = -INFINITY;
+        for (int t = 0; t < n; ++t) {
+            double dot = 0.0;
+            for (int k = 0; k < head_dim; ++k)
+                dot += widen(q_row[k], dtype) * keys[(size_t)t * head_dim + k];
+            scores[t] = scale * dot;
+            if (scores[t] > m) m = scores[t];
+        }
+        /* pass 2: exp(s - max), normaliser and weighted sum of values */
+        double denominator = 0.0;
+        double *o = out_group + (size_t)i * head_dim;
+        for (int k = 0; k < head_dim; ++k) o[k] = 0.0;
+        for (int t = 0; t < n; ++t) {
+            double p = exp(scores[t] - m);
+            denominator += p;
+            for (int k = 0; k < head_dim; ++k) o[k] += p * values[(size_t)t * head_dim + k];
+        }
+        for (int k = 0; k < head_dim; ++k) o[k] /= denominator;
+    }
+}
+
+/* Pools of 16-bit scalars (fp8 == 0) or of E4M3 codes with scale factors
+ * k_factor / v_factor (fp8 == 1). */
+static int paged_attention(const uint16_t *q, int dtype, int num_seqs, int num_q_heads,
+                           const void *k_cache, const void *v_cache, int fp8, double k_factor,
+                           double v_factor, int num_blocks, int num_kv_heads, int block_size,
+                           int head_dim, const int32_t *block_tables, int max_blocks_per_seq,
                            const int32_t *seq_lens, double scale, double *out, int num_threads) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0 ||
         head_dim <= 0 || (dtype != 0 && dtype != 1))
@@ -144,42 +245,52 @@ int oracle_paged_attention(const uint16_t *q, int dtype, int num_seqs, int num_q
             continue;
         }
         const int32_t *table_row = block_tables + (size_t)s * max_blocks_per_seq;
-        int gk = gather_contiguous(k_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim,
+        int gk, gv;
+        if (fp8) {
+            gk = gather_contiguous_e4m3(k_cache, k_factor, num_blocks, num_kv_heads, block_size,
+                                        head_dim, table_row, n, h, keys);
+            gv = gather_contiguous_e4m3(v_cache, v_factor, num_blocks, num_kv_heads, block_size,
+                                        head_dim, table_row, n, h, values);
+        } else {
+            gk = gather_contiguous(k_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim,
                                    table_row, n, h, keys);
-        int gv = gather_contiguous(v_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim,
+            gv = gather_contiguous(v_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim,
                                    table_row, n, h, values);
+        }
         if (gk != ORACLE_OK || gv != ORACLE_OK) {
             free(keys); free(values); free(scores);
 #pragma omp atomic write
             status = ORACLE_BAD_INDEX;
             continue;
         }
-        for (int i = 0; i < group; ++i) {
-            const int qh = h * group + i;
-            const uint16_t *q_row = q + ((size_t)s * num_q_heads + qh) * head_dim;
-            /* pass 1: scaled scores and their maximum */
-            double m = -INFINITY;
-            for (int t = 0; t < n; ++t) {
-                double dot = 0.0;
-                for (int k = 0; k < head_dim; ++k)
-                    dot += widen(q_row[k], dtype) * keys[(size_t)t * head_dim + k];
-                scores[t] = scale * dot;
-                if (scores[t] > m) m = scores[t];
-            }
-            /* pass 2: exp(s - max), normaliser and weighted sum of values */
-            double denominator = 0.0;
-            double *o = out_group + (size_t)i * head_dim;
-            for (int k = 0; k < head_dim; ++k) o[k] = 0.0;
-            for (int t = 0; t < n; ++t) {
-                double p = exp(scores[t] - m);
-                denominator += p;
-                for (int k = 0; k < head_dim; ++k) o[k] += p * values[(size_t)t * head_dim + k];
-            }
-            for (int k = 0; k < head_dim; ++k) o[k] /= denominator;
-        }
+        attend_group(q, dtype, s, h, group, num_q_heads, head_dim, n, keys, values, scores, scale,
+                     out_group);
         free(keys); free(values); free(scores);
     }
     return status;
+}
+
+int oracle_paged_attention(const uint16_t *q, int dtype, int num_seqs, int num_q_heads,
+                           const uint16_t *k_cache, const uint16_t *v_cache, int num_blocks,
+                           int num_kv_heads, int block_size, int head_dim,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, double scale, double *out, int num_threads) {
+    return paged_attention(q, dtype, num_seqs, num_q_heads, k_cache, v_cache, 0, 1.0, 1.0,
+                           num_blocks, num_kv_heads, block_size, head_dim, block_tables,
+                           max_blocks_per_seq, seq_lens, scale, out, num_threads);
+}
+
+/* The same attention over pools of E4M3 codes: key t of the formula is
+ * k_scale * decode(code), value t is v_scale * decode(code). */
+int oracle_paged_attention_fp8(const uint16_t *q, int dtype, int num_seqs, int num_q_heads,
+                               const uint8_t *k_cache, const uint8_t *v_cache, int num_blocks,
+                               int num_kv_heads, int block_size, int head_dim,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, double scale, float k_scale,
+                               float v_scale, double *out, int num_threads) {
+    return paged_attention(q, dtype, num_seqs, num_q_heads, k_cache, v_cache, 1, (double)k_scale,
+                           (double)v_scale, num_blocks, num_kv_heads, block_size, head_dim,
+                           block_tables, max_blocks_per_seq, seq_lens, scale, out, num_threads);
 }
 
 /* ------------------------------------------------------------------ */
@@ -370,6 +481,37 @@ int oracle_kv_write(const uint16_t *k, const uint16_t *v, const int64_t *slot_ma
             for (int e = 0; e < head_dim; ++e) {
                 k_cache[dst + e] = k[src + e];
                 v_cache[dst + e] = v[src + e];
+            }
+        }
+    }
+    return status;
+}
+
+/* The same slot write into pools of E4M3 codes: element x of a key row is
+ * stored as E4M3(x / k_scale), the quotient taken in binary32 (x is exact
+ * in binary32), and values likewise with v_scale. */
+int oracle_kv_write_fp8(const uint16_t *k, const uint16_t *v, int dtype,
+                        const int64_t *slot_mapping, int num_tokens, uint8_t *k_cache,
+                        uint8_t *v_cache, int num_blocks, int num_kv_heads, int block_size,
+                        int head_dim, float k_scale, float v_scale) {
+    if (dtype != 0 && dtype != 1) return ORACLE_BAD_ARG;
+    int status = ORACLE_OK;
+    for (int t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_blocks * block_size) { status = ORACLE_BAD_INDEX; continue; }
+        const int64_t physical = slot / block_size;
+        const int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+            const size_t dst = (((size_t)physical * num_kv_heads + h) * block_size + offset) * head_dim;
+            for (int e = 0; e < head_dim; ++e) {
+                const float kx = (float)widen(k[src + e], dtype);
+                const float vx = (float)widen(v[src + e], dtype);
+                const float k_quotient = kx / k_scale;
+                const float v_quotient = vx / v_scale;
+                k_cache[dst + e] = oracle_e4m3_from_f32(k_quotient);
+                v_cache[dst + e] = oracle_e4m3_from_f32(v_quotient);
             }
         }
     }

@@ -431,4 +431,178 @@ def pin_prefill_brute_force_against_library_softmax():
                 assert np.allclose(out[cu[s] + i, qh], w @ V, rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------
+# 8-bit (E4M3) pools: code = E4M3(x / scale) from the binary32 quotient,
+# read back as code * scale
+# ---------------------------------------------------------------------------
+def e4m3_values():
+    """Value of every E4M3 code through torch's float8_e4m3fn (a library conversion)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def e4m3_codes(x):
+    """binary32 values (|x| <= 448) -> E4M3 codes through torch (round to nearest even)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_decode_all_codes():
+    ref = e4m3_values()
+    got = np.array([oracle.e4m3_to_f64(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+    # the format's landmarks: largest finite 448 (S.1111.110), smallest normal
+    # 2^-6, smallest subnormal 2^-9, NaN only at S.1111.111
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9
+    assert got[0x38] == 1.0 and got[0xB8] == -1.0
+    assert set(np.flatnonzero(np.isnan(got)).tolist()) == {0x7F, 0xFF}
+
+
+def pin_e4m3_encode_round_trip_and_ties():
+    vals = e4m3_values()
+    for c in range(256):
+        if c not in (0x7F, 0xFF):
+            assert oracle.e4m3_from_f32(vals[c]) == c, hex(c)
+    for c in range(0x7E):  # neighbouring positive codes c, c + 1
+        mid = np.float32((vals[c] + vals[c + 1]) / 2)  # exact: at most 5 significant bits
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_from_f32(mid) == even and oracle.e4m3_from_f32(-mid) == 0x80 | even
+        below = np.nextafter(mid, np.float32(0))
+        above = np.nextafter(mid, np.float32(np.inf))
+        assert oracle.e4m3_from_f32(below) == c and oracle.e4m3_from_f32(above) == c + 1
+
+
+def pin_e4m3_encode_against_library_and_saturation():
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(20000) * 10.0 ** rng.uniform(-4.0, 2.6, 20000)).astype(np.float32)
+    x = x[np.abs(x) <= 464]  # torch turns larger magnitudes into NaN instead of saturating
+    got = np.array([oracle.e4m3_from_f32(v) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, e4m3_codes(x))
+    for v, code in ((465.0, 0x7E), (1e30, 0x7E), (np.inf, 0x7E), (-np.inf, 0xFE), (-1000.0, 0xFE),
+                    (0.0, 0x00), (-0.0, 0x80)):
+        assert oracle.e4m3_from_f32(v) == code, (v, code)
+    assert oracle.e4m3_from_f32(np.nan) == 0x7F
+
+
+def pin_kv_write_fp8_codes():
+    """Slots as kv_write; every element stored as E4M3 of the binary32 x / scale."""
+    rng = np.random.default_rng(32)
+    H, d, B, nb = 2, 8, 4, 5
+    k_scale, v_scale = 0.0371, 3.3
+    for dtype in ("float16", "bfloat16"):
+        k = to_bits(rng.standard_normal((3, H, d)) * 4, dtype)
+        v = to_bits(rng.standard_normal((3, H, d)) * 4, dtype)
+        kc = np.zeros((nb, H, B, d), dtype=np.uint8)
+        vc = np.zeros_like(kc)
+        kc2, vc2, status = oracle.kv_write_fp8(k, v, dtype, [6, -1, 19], kc, vc, k_scale, v_scale)
+        assert status == 0
+
+        def expect(bits, scale):
+            quotient = widen(bits, dtype).astype(np.float32) / np.float32(scale)  # binary32
+            return e4m3_codes(np.clip(quotient, -448, 448))
+
+        assert np.array_equal(kc2[1, :, 2], expect(k[0], k_scale))
+        assert np.array_equal(vc2[1, :, 2], expect(v[0], v_scale))
+        assert np.array_equal(kc2[4, :, 3], expect(k[2], k_scale))
+        assert np.array_equal(vc2[4, :, 3], expect(v[2], v_scale))
+        untouched = np.ones(nb, dtype=bool)
+        untouched[[1, 4]] = False
+        assert not kc2[untouched].any() and not vc2[untouched].any()
+        assert not kc2[1, :, [0, 1, 3]].any() and not kc2[4, :, :3].any()
+    # hand values, keys at scale 0.5: 1 / 0.5 = 2 = 1.0 * 2^(8-7) -> 0x40; -3 / 0.5 = -1.5 * 2^(9-7)
+    # -> 0xcc; 1000 / 0.5 saturates to 448 -> 0x7e.  Values at scale 1: 1 -> 0x38, -3 -> 0xc4.
+    one = to_bits(np.array([[[1.0, -3.0, 1000.0, 0.0]]]), "bfloat16")
+    kc2, vc2, _ = oracle.kv_write_fp8(one, one, "bfloat16", [0], np.zeros((1, 1, 1, 4), np.uint8),
+                                      np.zeros((1, 1, 1, 4), np.uint8), 0.5, 1.0)
+    assert kc2[0, 0, 0].tolist() == [0x40, 0xCC, 0x7E, 0x00]
+    assert vc2[0, 0, 0].tolist() == [0x38, 0xC4, 0x7E, 0x00]
+    _, _, status = oracle.kv_write_fp8(one, one, "bfloat16", [1], np.zeros((1, 1, 1, 4), np.uint8),
+                                       np.zeros((1, 1, 1, 4), np.uint8), 1.0, 1.0)
+    assert status != 0  # slot past the pool
+
+
+def pin_kv_write_fp8_rounds_the_binary32_quotient():
+    """Where the binary32 quotient lands exactly on a midpoint of two codes but
+    the exact quotient does not, the stored code follows the binary32 value."""
+    from fractions import Fraction
+    vals = e4m3_values()
+
+    def exact_nearest(q):
+        best = min(range(0x7F), key=lambda c: (abs(Fraction(float(vals[c])) - q), c % 2))
+        return best
+
+    differ = 0
+    for x in (1.0, 1.5, 3.0, 0.75):
+        for c in range(0x30, 0x48):
+            mid = (Fraction(float(vals[c])) + Fraction(float(vals[c + 1]))) / 2
+            s0 = np.float32(float(Fraction(x) / mid))
+            for s in (np.nextafter(s0, np.float32(0)), s0, np.nextafter(s0, np.float32(np.inf))):
+                k = to_bits(np.array([[[x]]]), "bfloat16")
+                kc, _, _ = oracle.kv_write_fp8(k, k, "bfloat16", [0], np.zeros((1, 1, 1, 1), np.uint8),
+                                               np.zeros((1, 1, 1, 1), np.uint8), float(s), 1.0)
+                binary32 = int(e4m3_codes([np.float32(x) / s])[0])
+                assert int(kc[0, 0, 0, 0]) == binary32, (x, float(s))
+                differ += binary32 != exact_nearest(Fraction(x) / Fraction(float(s)))
+    assert differ > 0  # the cases above do separate the two readings
+
+
+def fp8_case(rng, lengths, H_q, H_kv, d, B, spare=2):
+    """Random E4M3 pools (NaN codes excluded) and scattered block tables."""
+    need = [max(1, -(-n // B)) for n in lengths]
+    nb = sum(need) + spare
+    perm = rng.permutation(nb)
+    tables, pos = [], 0
+    for n in need:
+        tables.append([int(b) for b in perm[pos:pos + n]])
+        pos += n
+    kc = rng.integers(0, 256, size=(nb, H_kv, B, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, size=(nb, H_kv, B, d)).astype(np.uint8)
+    for pool in (kc, vc):
+        pool[(pool & 0x7F) == 0x7F] = 0x3C
+        pool[(pool & 0x78) >= 0x60] &= 0xC7  # keep magnitudes small: exponent field below 12
+    bt = np.zeros((len(lengths), max(need)), dtype=np.int32)
+    for s, t in enumerate(tables):
+        bt[s, :len(t)] = t
+    return kc, vc, bt, np.asarray(lengths, dtype=np.int32), tables
+
+
+def pin_fp8_attention_equals_16bit_on_the_same_values():
+    """With power-of-two scales the read-back values are exact in bfloat16, so
+    attention over the codes equals attention over those bfloat16 values."""
+    rng = np.random.default_rng(33)
+    kc, vc, bt, lens, _ = fp8_case(rng, [1, 7, 20], 4, 2, 16, 4)
+    vals = e4m3_values()
+    k16 = to_bits(vals[kc] * 2.0, "bfloat16")
+    v16 = to_bits(vals[vc] * 0.25, "bfloat16")
+    assert np.array_equal(widen(k16, "bfloat16"), vals[kc] * 2.0)
+    q = to_bits(rng.standard_normal((3, 4, 16)), "bfloat16")
+    a = oracle.attention_fp8(q, kc, vc, bt, lens, 0.3, 2.0, 0.25, "bfloat16")
+    b = oracle.attention(q, k16, v16, bt, lens, 0.3, "bfloat16")
+    assert np.array_equal(a, b)
+
+
+def pin_fp8_attention_brute_force_against_library_softmax():
+    rng = np.random.default_rng(34)
+    k_scale, v_scale = 0.0371, 3.3
+    vals = e4m3_values()
+    for dtype in ("float16", "bfloat16"):
+        kc, vc, bt, lens, tables = fp8_case(rng, [0, 1, 5, 9], 4, 2, 8, 4)
+        q = to_bits(rng.standard_normal((4, 4, 8)), dtype)
+        out = oracle.attention_fp8(q, kc, vc, bt, lens, 0.5, k_scale, v_scale, dtype)
+        assert not out[0].any()
+        for s, n in enumerate(lens):
+            for i in range(4):
+                h = i // 2
+                K = np.stack([vals[kc[tables[s][t // 4], h, t % 4]] for t in range(n)]) if n else None
+                if n == 0:
+                    continue
+                V = np.stack([vals[vc[tables[s][t // 4], h, t % 4]] for t in range(n)])
+                w = softmax(0.5 * ((K * np.float64(np.float32(k_scale))) @ widen(q[s, i], dtype)))
+                ref = w @ (V * np.float64(np.float32(v_scale)))
+                assert np.allclose(out[s, i], ref, rtol=1e-12, atol=1e-13)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -22,7 +22,7 @@ MUTANTS = {
                            "for (int k = 0; k < head_dim; ++k) o[k] /= 1.0;"),
     "dropped_scale": ("scores[t] = scale * dot;", "scores[t] = dot;"),
     "gqa_head_mapping": ("const int qh = h * group + i;",
-                         "const int qh = i * num_kv_heads + h;"),
+                         "const int qh = i * (num_q_heads / group) + h;"),
     "gather_block_index": ("int32_t physical = table_row[t / block_size];\n        int slot = t % block_size;",
                            "int32_t physical = table_row[t % block_size];\n        int slot = t / block_size;"),
     "gather_slot_off_by_one": ("int slot = t % block_size;", "int slot = (t + 1) % block_size;"),
@@ -50,6 +50,20 @@ MUTANTS = {
     "prefill_sees_the_future": ("const int visible = ctx + i + 1;", "const int visible = n;"),
     "prefill_query_row": ("const size_t row = ((size_t)(cu_q[s] + i) * num_q_heads + qh) * head_dim;",
                           "const size_t row = ((size_t)(cu_q[s] + i) * num_q_heads + h) * head_dim;"),
+    "e4m3_exponent_bias": ("ldexp((double)(8 + mantissa), exponent - 10)",
+                           "ldexp((double)(8 + mantissa), exponent - 9)"),
+    "e4m3_subnormal_scale": ("magnitude = ldexp((double)mantissa, -9);",
+                             "magnitude = ldexp((double)mantissa, -10);"),
+    "e4m3_ties_away": ("(remainder == 0.5 && fmod(r, 2.0) == 1.0)", "(remainder == 0.5)"),
+    "e4m3_overflow_to_nan": ("if (a >= 448.0) return sign | 0x7e;", "if (a >= 448.0) return sign | 0x7f;"),
+    "e4m3_binade_off_by_one": ("e = exponent - 1;", "e = exponent;"),
+    "fp8_write_multiplies_scale": ("const float k_quotient = kx / k_scale;",
+                                   "const float k_quotient = kx * k_scale;"),
+    "fp8_write_value_scale_swapped": ("const float v_quotient = vx / v_scale;",
+                                      "const float v_quotient = vx / k_scale;"),
+    "fp8_read_drops_scale": ("dst[(size_t)t * head_dim + k] = factor * oracle_e4m3_to_f64(row[k]);",
+                             "dst[(size_t)t * head_dim + k] = oracle_e4m3_to_f64(row[k]);"),
+    "fp8_read_value_scale_from_keys": ("(double)v_scale, num_blocks", "(double)k_scale, num_blocks"),
     "empty_sequence_nonzero": ("for (size_t e = 0; e < (size_t)group * head_dim; ++e) out_group[e] = 0.0;",
                                "for (size_t e = 0; e < (size_t)group * head_dim; ++e) out_group[e] = 1.0;"),
 }

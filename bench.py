@@ -66,11 +66,11 @@ def parse_args():
 # ----------------------------------------------------------------------------
 # accounting
 # ----------------------------------------------------------------------------
-def attention_bytes(step) -> int:
-    """Algorithmic bytes of one paged_decode_attention call."""
+def attention_bytes(step, kv_scalar_bytes: int = 2) -> int:
+    """Algorithmic bytes of one paged_decode_attention call (1-byte scalars: 8-bit pools)."""
     lens = step.seq_lens.to(torch.int64)
-    b = 2  # bytes per scalar
-    kv = int(lens.sum()) * step.num_kv_heads * step.head_dim * b * 2
+    b = 2  # bytes per scalar of q and out
+    kv = int(lens.sum()) * step.num_kv_heads * step.head_dim * kv_scalar_bytes * 2
     qo = 2 * step.num_seqs * step.num_q_heads * step.head_dim * b
     tables = int(((lens + step.block_size - 1) // step.block_size).sum()) * 4 + 4 * step.num_seqs
     return kv + qo + tables
@@ -307,6 +307,52 @@ def measure_attention(pkv, step, device, label, workload):
             "decode_tokens_per_s": round(step.num_seqs / (ms * 1e-3), 1)}
 
 
+# Scales of the 8-bit pools: N(0, 1) keys / values map onto about +-4.8 / +-4.0.
+FP8_K_SCALE, FP8_V_SCALE = 0.0107, 0.0089
+
+
+def measure_attention_fp8(pkv, step, device, workload, reps=200, warmup=10):
+    """Decode attention over 8-bit (E4M3) pools quantised from the step's 16-bit pools."""
+    nb, h, b, d = step.k_cache.shape
+    kc8 = torch.empty((nb, h, b, d), dtype=torch.uint8, device=device)
+    vc8 = torch.empty_like(kc8)
+    slots = torch.arange(nb * b, dtype=torch.int64, device=device)
+    rows = [pool.permute(0, 2, 1, 3).reshape(nb * b, h, d).contiguous().to(device)
+            for pool in (step.k_cache, step.v_cache)]  # every slot, in slot order
+    pkv.kv_write_fp8(rows[0], rows[1], slots, kc8, vc8, FP8_K_SCALE, FP8_V_SCALE)
+    del rows
+    q = step.q.to(device)
+    bt, sl = step.block_tables.to(device), step.seq_lens.to(device)
+    ws = torch.zeros(max(pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads,
+                                                     step.max_seq_len, step.block_size, 0), 16),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty_like(q)
+
+    def call():
+        pkv.paged_decode_attention_fp8(q, kc8, vc8, bt, sl, FP8_K_SCALE, FP8_V_SCALE, step.scale,
+                                       out, max_seq_len=step.max_seq_len, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    hbm, kind = measured_peaks()
+    gbs = attention_bytes(step, 1) / (ms * 1e-3) / 1e9
+    del kc8, vc8, q, bt, sl, ws, out
+    torch.cuda.empty_cache()
+    return {"workload": workload, "kv_format": "E4M3 codes, one scale per pool",
+            "attention_ms": round(ms, 4), "achieved_gbs": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / hbm, 4), "peak_kind": kind,
+            "decode_tokens_per_s": round(step.num_seqs / (ms * 1e-3), 1)}
+
+
 def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
     """Full decode steps (copy-on-write copies + kv_write + attention) of the
     prefix-sharing scenario, all 256 steps' inputs resident on the device."""
@@ -449,7 +495,14 @@ def other_workloads(pkv, W, device, all_configs):
     extra = {"long_context": measure_attention(
         pkv, W.long_context(), device, "long_context",
         "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16"),
-        "prefill": measure_prefill(pkv, W, device)}
+        "prefill": measure_prefill(pkv, W, device),
+        "gqa_fp8": measure_attention_fp8(
+            pkv, W.gqa_batch(), device,
+            "GQA decode batch over 8-bit pools: 64 sequences 512..4096, 32 q / 8 kv heads, "
+            "bf16 queries, block 16"),
+        "long_context_fp8": measure_attention_fp8(
+            pkv, W.long_context(), device,
+            "8 sequences x 32768 tokens over 8-bit pools, 32 q / 8 kv heads, bf16 queries")}
     if all_configs:
         for bs in (16, 32):
             st = W.tiny(bs)

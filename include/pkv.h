@@ -34,6 +34,10 @@
  *    caller reads the flag after synchronising the stream.
  *  - Calls on the same stream execute in order; calls that touch the same
  *    cache from different streams must be ordered by the caller.
+ *  - pkv_kv_write, pkv_kv_write_layers, pkv_paged_decode_attention (and its
+ *    fixed-scratch form) and pkv_paged_prefill_attention work on 16-bit
+ *    pools: c.dtype PKV_FP8_E4M3 returns PKV_ERR_INVALID_ARG there (the
+ *    *_fp8 calls serve 8-bit pools).
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -59,7 +63,10 @@ typedef enum {
     PKV_ERR_CUDA = 4                  /* a CUDA launch or driver call failed */
 } pkv_status;
 
-typedef enum { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* Scalar types.  PKV_FP8_E4M3 is a storage type of pools only (see
+ * "8-bit pools" below); queries, new keys / values and outputs are
+ * PKV_FP16 or PKV_BF16. */
+typedef enum { PKV_FP16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 
 /* Bits ORed into *err_flag by the kernels (device-side data errors). */
 #define PKV_DEVERR_BAD_SLOT     1  /* slot_mapping[t] >= num_blocks * block_size */
@@ -74,7 +81,8 @@ typedef struct {
     int32_t num_kv_heads;  /* KV heads, > 0 */
     int32_t block_size;    /* token slots per block */
     int32_t head_dim;      /* scalars per head */
-    pkv_dtype dtype;       /* storage type of caches, q, k, v and out */
+    pkv_dtype dtype;       /* storage type of the pools; for the 16-bit calls also the
+                              type of q, k, v and out (PKV_FP16 or PKV_BF16 there) */
 } pkv_cache_desc;
 
 /*
@@ -248,6 +256,8 @@ PKV_API pkv_status pkv_paged_decode_attention_fixed_scratch(
  *     k_cache[dst_p] = k_cache[src_p],  v_cache[dst_p] = v_cache[src_p]
  * over every KV head and every slot, filled or not, bit for bit.
  *
+ *   c              any storage dtype, PKV_FP8_E4M3 included (blocks are
+ *                  copied as bytes).
  *   src_dst_pairs  DEVICE [num_pairs][2] int64 (src, dst).  Destinations
  *                  must be distinct and no destination may be the source of
  *                  another pair (pairs run concurrently).  A pair with an
@@ -274,8 +284,8 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc 
  *                 writes host pools directly over the CPU-GPU link, one launch
  *                 for all pairs.  Pageable host memory is rejected with
  *                 PKV_ERR_INVALID_ARG.  The two pairs of pools must not overlap.
- *   c             shared geometry (num_kv_heads, block_size, head_dim, dtype);
- *                 its num_blocks is not used.
+ *   c             shared geometry (num_kv_heads, block_size, head_dim, dtype,
+ *                 PKV_FP8_E4M3 included); its num_blocks is not used.
  *   src_dst_pairs DEVICE [num_pairs][2] int64 (src block, dst block).
  *                 Destinations must be distinct.  A pair outside either pool
  *                 is skipped and sets PKV_DEVERR_BAD_PAIR.
@@ -306,12 +316,78 @@ PKV_API pkv_status pkv_kv_write_layers(const void* const* k, const void* const* 
  * pkv_copy_blocks for num_layers layers in one launch: the same (src, dst)
  * pairs are applied to every layer's k_caches[l], v_caches[l] (HOST arrays
  * of num_layers device pointers).  1 <= num_layers <= PKV_MAX_LAYERS.
- * Errors and conventions as pkv_copy_blocks.
+ * Errors and conventions as pkv_copy_blocks (any storage dtype).
  */
 PKV_API pkv_status pkv_copy_blocks_layers(void* const* k_caches, void* const* v_caches,
                                           int32_t num_layers, pkv_cache_desc c,
                                           const int64_t* src_dst_pairs, int32_t num_pairs,
                                           int32_t* err_flag, void* stream);
+
+/*
+ * 8-bit pools (c.dtype == PKV_FP8_E4M3).
+ *
+ * The pages note that the key-value cache need not share the model's
+ * precision and that changing it changes the numerics ("Serving Language
+ * Models Within a Memory Budget", section 4, "Allocation efficiency is not
+ * the entire memory budget").  This library's 8-bit format: each stored
+ * scalar is one byte in the OCP FP8 E4M3 encoding (1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN,
+ * largest finite magnitude 448), and each pool has one scale factor, k_scale
+ * for the key pool and v_scale for the value pool.  A scalar x is stored as
+ * E4M3(x / scale), the quotient taken in binary32 and rounded to the nearest
+ * code (ties to even), magnitudes above 448 saturating to 448; the code is
+ * read back as code * scale.  Layout as the 16-bit pools with one-byte
+ * scalars: [num_blocks][num_kv_heads][block_size][head_dim] bytes.  The
+ * block copies (pkv_copy_blocks, pkv_swap_blocks, pkv_copy_blocks_layers)
+ * take such pools as they are.
+ */
+
+/*
+ * pkv_kv_write into 8-bit pools: the key row of token t, KV head h is stored
+ * at slot slot_mapping[t] as E4M3(k[t][h][:] / k_scale), and values with
+ * v_scale.
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim] of kv_dtype (PKV_FP16
+ *                 or PKV_BF16), contiguous, 16-byte aligned.
+ *   k_cache, v_cache  pools of E4M3 codes; c.dtype must be PKV_FP8_E4M3.
+ *   k_scale, v_scale  finite and > 0.
+ * Slots, padding, errors and head_dim rules as pkv_kv_write (head_dim a
+ * multiple of 16 here).  Non-finite inputs: infinities saturate to +-448,
+ * NaN is stored as 0x7f.
+ */
+PKV_API pkv_status pkv_kv_write_fp8(const void* k, const void* v, pkv_dtype kv_dtype,
+                                    const int64_t* slot_mapping, int32_t num_tokens,
+                                    void* k_cache, void* v_cache, pkv_cache_desc c, float k_scale,
+                                    float v_scale, int32_t* err_flag, void* stream);
+
+/*
+ * pkv_paged_decode_attention over 8-bit pools:
+ *     out[s][i] = sum_t softmax_t(scale * q[s][i] . (k_scale * Kc_t)) (v_scale * Vc_t)
+ * where Kc_t, Vc_t are the decoded E4M3 codes of token t.  The codes are
+ * widened exactly to binary16 and multiplied with binary16 queries; a
+ * bfloat16 query row is first multiplied by a power of two that brings its
+ * largest magnitude into [2^14, 2^15) and rounded to binary16, the power of
+ * two being divided out of its scores.  Products accumulate in fp32; the
+ * output is rounded to q_dtype.
+ *
+ *   q, out        [num_seqs][num_q_heads][head_dim] of q_dtype (PKV_FP16 or
+ *                 PKV_BF16).
+ *   k_cache, v_cache  E4M3 pools (c.dtype == PKV_FP8_E4M3), 16-byte aligned.
+ *   k_scale, v_scale  the pools' scales, finite and > 0.
+ *   workspace     >= pkv_decode_workspace_bytes(num_seqs, num_q_heads,
+ *                 head_dim, max_seq_len, block_size, 0) bytes.
+ * Other arguments, errors and the empty-sequence rule as
+ * pkv_paged_decode_attention in automatic mode.  Supported: head_dim 128,
+ * block_size 8, 16, 32, 64 or 128, num_q_heads / num_kv_heads <= 16,
+ * num_seqs <= 4096 (the streaming kernel); other valid shapes return
+ * PKV_ERR_UNSUPPORTED.
+ */
+PKV_API pkv_status pkv_paged_decode_attention_fp8(
+    const void* q, pkv_dtype q_dtype, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+    int32_t max_seq_len, int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c, float scale,
+    float k_scale, float v_scale, void* workspace, size_t workspace_bytes, void* out,
+    int32_t* err_flag, void* stream);
 
 /* Static, NUL-terminated name of a status code. */
 PKV_API const char* pkv_status_string(pkv_status status);

@@ -14,7 +14,10 @@ behind the C ABI of ``libpkv.so`` (``include/pkv.h``), do the work:
 * ``swap_blocks``            block copies between device and page-locked host
                              pools (preemption by swap);
 * ``kv_write_layers`` / ``copy_blocks_layers``  the same for every layer of a
-                             model in one launch.
+                             model in one launch;
+* ``kv_write_fp8`` / ``paged_decode_attention_fp8``  the slot write and the
+                             decode attention over 8-bit pools (E4M3 codes
+                             with one scale per pool).
 
 ``block_manager`` is the host-side block table / refcount manager that
 produces the kernels' inputs; ``workloads`` generates seeded synthetic
@@ -23,8 +26,10 @@ decode batches.
 from ._lib import PKVError  # noqa: F401
 from .ops import (cache_desc, copy_blocks, copy_blocks_layers,  # noqa: F401
                   decode_partition_size, decode_workspace_bytes, kv_write, kv_write_layers,
-                  paged_decode_attention, paged_prefill_attention, swap_blocks)
+                  kv_write_fp8, paged_decode_attention, paged_decode_attention_fp8,
+                  paged_prefill_attention, swap_blocks)
 
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
            "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
-           "copy_blocks_layers", "paged_prefill_attention"]
+           "copy_blocks_layers", "paged_prefill_attention", "kv_write_fp8",
+           "paged_decode_attention_fp8"]

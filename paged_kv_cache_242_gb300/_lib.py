@@ -12,7 +12,7 @@ from .build import LIBRARY
 PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 3: "PKV_ERR_WORKSPACE_TOO_SMALL", 4: "PKV_ERR_CUDA"}
-PKV_FP16, PKV_BF16 = 0, 1
+PKV_FP16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 MAX_LAYERS = 128
 
 DEVERR_BAD_SLOT = 1
@@ -64,6 +64,14 @@ def _declare(lib):
     lib.pkv_kv_write_layers.restype = ctypes.c_int
     lib.pkv_copy_blocks_layers.argtypes = [ptrs, ptrs, i32, CacheDesc, vp, i32, i32p, vp]
     lib.pkv_copy_blocks_layers.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.pkv_kv_write_fp8.argtypes = [vp, vp, ctypes.c_int, vp, i32, vp, vp, CacheDesc, f32, f32,
+                                     i32p, vp]
+    lib.pkv_kv_write_fp8.restype = ctypes.c_int
+    lib.pkv_paged_decode_attention_fp8.argtypes = [vp, ctypes.c_int, vp, vp, vp, i32, vp, i32, i32,
+                                                   i32, CacheDesc, f32, f32, f32, vp,
+                                                   ctypes.c_size_t, vp, i32p, vp]
+    lib.pkv_paged_decode_attention_fp8.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_abi_version.argtypes = []

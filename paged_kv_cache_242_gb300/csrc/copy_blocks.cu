@@ -60,7 +60,7 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_des
                                cudaStream_t stream) {
     if (num_pairs == 0) return cudaSuccess;
     const int64_t vecs_per_block =
-        static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
+        static_cast<int64_t>(c.num_kv_heads) * c.block_size * row_vectors(c);
     const int64_t chunks = (vecs_per_block + kVecsPerCta - 1) / kVecsPerCta;
     dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(chunks));
     return launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, stream,

@@ -20,9 +20,11 @@
 // combines by the same Eq. (4) rule.
 //
 // Pipeline.  Each warp owns kStreamStages (2) 8 KiB shared-memory stages
-// (K and V of one tile, two 64-column boxes each, 128-byte swizzle).  Lane 0
-// issues the TMA loads of tile k + 2 as soon as the warp has finished tile k,
-// so 14 tiles per SM are in flight or being consumed.  (Sweeps of warps x
+// (K and V of one tile, two 64-column boxes each, 128-byte swizzle); over
+// 8-bit (E4M3) pools, kStreamStagesFp8 (4) stages of 4 KiB (one 128-byte
+// box per tile) and the per-tile math of attend_tile_e4m3.  Lane 0
+// issues the TMA loads of tile k + stages as soon as the warp has finished
+// tile k, so 16-bit pools keep 14 tiles per SM in flight or being consumed.  (Sweeps of warps x
 // stages on GB300 put the optimum at 7-8 warps x 2 stages: more requests in
 // flight only queue at the saturated HBM.)  Block-table entries are fetched
 // 32 at a time by the whole warp.  The per-tile math is
@@ -37,12 +39,20 @@
 namespace pkv {
 namespace {
 
-constexpr int kStages = kStreamStages;
-constexpr int kStageBytes = 4 * kTileTokens * 128;  // K and V, two halves each: 8 KiB
-constexpr int kHalf = kTileTokens * 128;             // one 64-column box of 16 rows
-constexpr int kRingBytes = kStreamWarps * kStages * kStageBytes;
+// Shared-memory layout of one warp's ring.  16-bit pools: a stage holds the
+// K and V tiles of 16 rows as two 64-column boxes each (8 KiB).  8-bit pools
+// (E4M3 codes): one 128-byte box per tile (4 KiB), twice the stages.
+template <bool kFp8>
+struct StreamLayout {
+    static constexpr int kStages = kFp8 ? kStreamStagesFp8 : kStreamStages;
+    static constexpr int kTileBytes = kTileTokens * kHeadDim * (kFp8 ? 1 : 2);  // K or V
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRingBytes = kStreamWarps * kStages * kStageBytes;
+};
+constexpr int kHalf = kTileTokens * 128;  // one 128-byte-wide box of 16 rows
 constexpr int kThreads = kStreamWarps * 32;
 
+template <int kStages>
 struct alignas(8) StreamControl {
     uint64_t full[kStreamWarps][kStages];
     int32_t valid[kStreamWarps][kStages];
@@ -88,14 +98,17 @@ __device__ __forceinline__ Cursor cursor_at(int64_t t, const int32_t* prefix, in
     return c;
 }
 
-template <typename T, int BS>
+template <typename T, int BS, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_stream_kernel(const __grid_constant__ CUtensorMap k_map,
                                const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+    using L = StreamLayout<kFp8>;
+    constexpr int kStages = L::kStages;
+    constexpr int kStageBytes = L::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    StreamControl* ctl = reinterpret_cast<StreamControl*>(ring + kRingBytes);
+    auto* ctl = reinterpret_cast<StreamControl<kStages>*>(ring + L::kRingBytes);
     int32_t* prefix = reinterpret_cast<int32_t*>(ctl + 1);  // [S + 1]
     int32_t* lens = prefix + a.num_seqs + 1;                // [S]
 
@@ -213,18 +226,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ctl->valid[warp][st] = ok ? 1 : 0;
             if (ok) {
                 const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
-                const uint32_t vt = kt + 2 * kHalf;
+                const uint32_t vt = kt + L::kTileBytes;
                 const int row = (iss.i * kTileTokens) % BS;  // 0 when BS <= 16
                 fence_proxy_async_shared();  // earlier generic reads of this stage
-                mbar_arrive_expect_tx(full, present * kBoxRows * 128 * 4);
+                mbar_arrive_expect_tx(full, present * kBoxRows * 128 * (kFp8 ? 2 : 4));
 #pragma unroll
                 for (int b = 0; b < kBlocksPerTile; ++b) {
                     if (blk + b < nblocks) {
                         const uint32_t off = b * kBoxRows * 128;
                         tma_load_4d(kt + off, &k_map, full, 0, row, iss.h, ids[b]);
-                        tma_load_4d(kt + kHalf + off, &k_map, full, 64, row, iss.h, ids[b]);
                         tma_load_4d(vt + off, &v_map, full, 0, row, iss.h, ids[b]);
-                        tma_load_4d(vt + kHalf + off, &v_map, full, 64, row, iss.h, ids[b]);
+                        if constexpr (!kFp8) {  // second 64-column half of 16-bit rows
+                            tma_load_4d(kt + kHalf + off, &k_map, full, 64, row, iss.h, ids[b]);
+                            tma_load_4d(vt + kHalf + off, &v_map, full, 64, row, iss.h, ids[b]);
+                        }
                     }
                 }
             } else {
@@ -244,12 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qa[8][4];
     float o[16][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float sl0 = a.scale_log2, sl1 = a.scale_log2;  // per-row score factors (8-bit pools)
 
     auto reset = [&]() {
         const T* q_rows = static_cast<const T*>(a.q) +
                           (static_cast<size_t>(cur.s) * a.num_q_heads + static_cast<size_t>(cur.h) * g) *
                               kHeadDim;
-        load_q_fragments<T>(qa, q_rows, g, lane);
+        if constexpr (kFp8)
+            load_q_fragments_e4m3<T>(qa, q_rows, g, lane, a.scale_log2, sl0, sl1);
+        else
+            load_q_fragments<T>(qa, q_rows, g, lane);
 #pragma unroll
         for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
         m0 = m1 = -INFINITY;
@@ -263,32 +282,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
         s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
         const size_t qrow = static_cast<size_t>(seg.s) * a.num_q_heads + static_cast<size_t>(seg.h) * g;
+        // 16-bit pools: n-tile nd holds dims nd * 8 + 2 quad + {0, 1}.  8-bit
+        // pools: n-tiles 2c and 2c + 1 interleave dims 16 c + 4 quad + {0..3}.
+        const float vs = kFp8 ? a.v_scale : 1.f;
         if (whole) {
-            const float inv0 = s0 > 0.f ? 1.f / s0 : 0.f;
-            const float inv1 = s1 > 0.f ? 1.f / s1 : 0.f;
+            const float inv0 = s0 > 0.f ? vs / s0 : 0.f;
+            const float inv1 = s1 > 0.f ? vs / s1 : 0.f;
             T* out = static_cast<T*>(a.out);
+            if constexpr (kFp8) {
 #pragma unroll
-            for (int nd = 0; nd < 16; ++nd) {
-                const int col = nd * 8 + quad * 2;
-                if (row0 < g)
-                    *reinterpret_cast<uint32_t*>(out + (qrow + row0) * kHeadDim + col) =
-                        Mma<T>::pack(o[nd][0] * inv0, o[nd][1] * inv0);
-                if (row0 + 8 < g)
-                    *reinterpret_cast<uint32_t*>(out + (qrow + row0 + 8) * kHeadDim + col) =
-                        Mma<T>::pack(o[nd][2] * inv1, o[nd][3] * inv1);
+                for (int c = 0; c < 8; ++c) {
+                    const int col = c * 16 + quad * 4;
+                    if (row0 < g)
+                        *reinterpret_cast<uint2*>(out + (qrow + row0) * kHeadDim + col) =
+                            make_uint2(Mma<T>::pack(o[2 * c][0] * inv0, o[2 * c + 1][0] * inv0),
+                                       Mma<T>::pack(o[2 * c][1] * inv0, o[2 * c + 1][1] * inv0));
+                    if (row0 + 8 < g)
+                        *reinterpret_cast<uint2*>(out + (qrow + row0 + 8) * kHeadDim + col) =
+                            make_uint2(Mma<T>::pack(o[2 * c][2] * inv1, o[2 * c + 1][2] * inv1),
+                                       Mma<T>::pack(o[2 * c][3] * inv1, o[2 * c + 1][3] * inv1));
+                }
+            } else {
+#pragma unroll
+                for (int nd = 0; nd < 16; ++nd) {
+                    const int col = nd * 8 + quad * 2;
+                    if (row0 < g)
+                        *reinterpret_cast<uint32_t*>(out + (qrow + row0) * kHeadDim + col) =
+                            Mma<T>::pack(o[nd][0] * inv0, o[nd][1] * inv0);
+                    if (row0 + 8 < g)
+                        *reinterpret_cast<uint32_t*>(out + (qrow + row0 + 8) * kHeadDim + col) =
+                            Mma<T>::pack(o[nd][2] * inv1, o[nd][3] * inv1);
+                }
             }
         } else {
             const int64_t pid = gw + static_cast<int64_t>(seg.s) * H + seg.h;
             const size_t rbase = static_cast<size_t>(pid) * g;
+            if constexpr (kFp8) {
 #pragma unroll
-            for (int nd = 0; nd < 16; ++nd) {
-                const int col = nd * 8 + quad * 2;
-                if (row0 < g)
-                    *reinterpret_cast<float2*>(a.ws_acc + (rbase + row0) * kHeadDim + col) =
-                        make_float2(o[nd][0], o[nd][1]);
-                if (row0 + 8 < g)
-                    *reinterpret_cast<float2*>(a.ws_acc + (rbase + row0 + 8) * kHeadDim + col) =
-                        make_float2(o[nd][2], o[nd][3]);
+                for (int c = 0; c < 8; ++c) {
+                    const int col = c * 16 + quad * 4;
+                    if (row0 < g)
+                        *reinterpret_cast<float4*>(a.ws_acc + (rbase + row0) * kHeadDim + col) =
+                            make_float4(o[2 * c][0] * vs, o[2 * c + 1][0] * vs, o[2 * c][1] * vs,
+                                        o[2 * c + 1][1] * vs);
+                    if (row0 + 8 < g)
+                        *reinterpret_cast<float4*>(a.ws_acc + (rbase + row0 + 8) * kHeadDim + col) =
+                            make_float4(o[2 * c][2] * vs, o[2 * c + 1][2] * vs, o[2 * c][3] * vs,
+                                        o[2 * c + 1][3] * vs);
+                }
+            } else {
+#pragma unroll
+                for (int nd = 0; nd < 16; ++nd) {
+                    const int col = nd * 8 + quad * 2;
+                    if (row0 < g)
+                        *reinterpret_cast<float2*>(a.ws_acc + (rbase + row0) * kHeadDim + col) =
+                            make_float2(o[nd][0], o[nd][1]);
+                    if (row0 + 8 < g)
+                        *reinterpret_cast<float2*>(a.ws_acc + (rbase + row0 + 8) * kHeadDim + col) =
+                            make_float2(o[nd][2], o[nd][3]);
+                }
             }
             if (quad == 0) {
                 if (row0 < g) {
@@ -319,8 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ctl->valid[warp][st]) {
             const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
             const int nvalid = min(kTileTokens, lens[cur.s] - cur.i * kTileTokens);
-            attend_block<T, kTileTokens, true>(kt, kt + 2 * kHalf, nvalid, qa, o, m0, m1, l0, l1,
-                                               a.scale_log2, lane);
+            if constexpr (kFp8)
+                attend_tile_e4m3<true>(kt, kt + L::kTileBytes, nvalid, qa, o, m0, m1, l0, l1, sl0,
+                                       sl1, lane);
+            else
+                attend_block<T, kTileTokens, true>(kt, kt + L::kTileBytes, nvalid, qa, o, m0, m1,
+                                                   l0, l1, a.scale_log2, lane);
         }
         __syncwarp();
         if (k + kStages < count) issue(k + kStages);
@@ -412,13 +468,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
     *ocol = make_uint2(Mma<T>::pack(acc.x * inv, acc.y * inv), Mma<T>::pack(acc.z * inv, acc.w * inv));
 }
 
-template <typename T, int BS>
+template <bool kFp8>
+constexpr size_t stream_smem_bytes(int num_seqs) {
+    return 1024 + StreamLayout<kFp8>::kRingBytes + sizeof(StreamControl<StreamLayout<kFp8>::kStages>) +
+           (2 * static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t);
+}
+
+template <typename T, int BS, bool kFp8>
 cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_map,
                                 const DecodeArgs& a, int ctas, cudaStream_t stream) {
-    const size_t smem = 1024 + kRingBytes + sizeof(StreamControl) +
-                        (2 * static_cast<size_t>(a.num_seqs) + 1) * sizeof(int32_t);
-    auto kernel = paged_decode_stream_kernel<T, BS>;
-    cudaError_t err = ensure_smem_limit<paged_decode_stream_kernel<T, BS>>(smem);
+    const size_t smem = stream_smem_bytes<kFp8>(a.num_seqs);
+    auto kernel = paged_decode_stream_kernel<T, BS, kFp8>;
+    cudaError_t err = ensure_smem_limit<paged_decode_stream_kernel<T, BS, kFp8>>(smem);
     if (err != cudaSuccess) return err;
     err = launch_pdl(kernel, dim3(ctas), dim3(kThreads), smem, stream, k_map, v_map, a);
     if (err != cudaSuccess) return err;
@@ -428,14 +489,55 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
                       dim3(kMergeWarps * 32), 0, stream, a);
 }
 
+template <typename T, bool kFp8>
+cudaError_t launch_stream_block(const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                const DecodeArgs& a, int block_size, int ctas,
+                                cudaStream_t stream) {
+    switch (block_size) {
+        case 8: return launch_stream_typed<T, 8, kFp8>(k_map, v_map, a, ctas, stream);
+        case 16: return launch_stream_typed<T, 16, kFp8>(k_map, v_map, a, ctas, stream);
+        case 32: return launch_stream_typed<T, 32, kFp8>(k_map, v_map, a, ctas, stream);
+        case 64: return launch_stream_typed<T, 64, kFp8>(k_map, v_map, a, ctas, stream);
+        default: return launch_stream_typed<T, 128, kFp8>(k_map, v_map, a, ctas, stream);
+    }
+}
+
+// Grid size and workspace carving shared by both pool formats.
+template <bool kFp8>
+cudaError_t launch_stream(const CUtensorMap& k_map, const CUtensorMap& v_map, DecodeArgs a,
+                          pkv_dtype dtype, int block_size, cudaStream_t stream) {
+    int device = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (err != cudaSuccess) return err;
+    // enough CTAs for ~16 tiles per warp, at most one per SM
+    const int64_t max_tiles = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
+                              ((a.max_seq_len + kTileTokens - 1) / kTileTokens);
+    int64_t ctas = (max_tiles + kStreamWarps * 16 - 1) / (kStreamWarps * 16);
+    const int cap = sms < kStreamMaxCtas ? sms : kStreamMaxCtas;
+    if (ctas > cap) ctas = cap;
+    if (ctas < 1) ctas = 1;
+    a.num_warps = static_cast<int32_t>(ctas) * kStreamWarps;
+    // workspace layout: acc [rows][128], m [rows], l [rows], prefix [S + 1]
+    const size_t rows = (static_cast<size_t>(a.num_warps) +
+                         static_cast<size_t>(a.num_seqs) * a.num_kv_heads) * a.group;
+    float* ws = a.ws_acc;
+    a.ws_m = ws + rows * kHeadDim;
+    a.ws_l = a.ws_m + rows;
+    a.ws_prefix = reinterpret_cast<int32_t*>(a.ws_l + rows);
+    return dtype == PKV_BF16
+               ? launch_stream_block<__nv_bfloat16, kFp8>(k_map, v_map, a, block_size, (int)ctas, stream)
+               : launch_stream_block<__half, kFp8>(k_map, v_map, a, block_size, (int)ctas, stream);
+}
+
 }  // namespace
 
 bool stream_supported(int num_seqs, int group, int block_size) {
     return num_seqs >= 1 && num_seqs <= kStreamMaxSeqs && group >= 1 && group <= 16 &&
            (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64 ||
             block_size == 128) &&
-           1024 + kRingBytes + sizeof(StreamControl) + (2 * static_cast<size_t>(num_seqs) + 1) * 4 <=
-               232448;
+           stream_smem_bytes<false>(num_seqs) <= 232448 && stream_smem_bytes<true>(num_seqs) <= 232448;
 }
 
 // Rows of partial statistics: one per (partial id, query head of the group);
@@ -459,44 +561,13 @@ size_t stream_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads_or
 cudaError_t launch_paged_decode_stream(const CUtensorMap& k_map16, const CUtensorMap& v_map16,
                                        DecodeArgs a, pkv_dtype dtype, int block_size,
                                        cudaStream_t stream) {
-    int device = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&device);
-    if (err != cudaSuccess) return err;
-    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (err != cudaSuccess) return err;
-    // enough CTAs for ~16 tiles per warp, at most one per SM
-    const int64_t max_tiles = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
-                              ((a.max_seq_len + kTileTokens - 1) / kTileTokens);
-    int64_t ctas = (max_tiles + kStreamWarps * 16 - 1) / (kStreamWarps * 16);
-    const int cap = sms < kStreamMaxCtas ? sms : kStreamMaxCtas;
-    if (ctas > cap) ctas = cap;
-    if (ctas < 1) ctas = 1;
-    a.num_warps = static_cast<int32_t>(ctas) * kStreamWarps;
-    // workspace layout: acc [rows][128], m [rows], l [rows], prefix [S + 1]
-    const size_t rows = (static_cast<size_t>(a.num_warps) +
-                         static_cast<size_t>(a.num_seqs) * a.num_kv_heads) * a.group;
-    float* ws = a.ws_acc;
-    a.ws_m = ws + rows * kHeadDim;
-    a.ws_l = a.ws_m + rows;
-    a.ws_prefix = reinterpret_cast<int32_t*>(a.ws_l + rows);
-    const bool bf16 = dtype == PKV_BF16;
-    switch (block_size) {
-        case 8:
-            return bf16 ? launch_stream_typed<__nv_bfloat16, 8>(k_map16, v_map16, a, (int)ctas, stream)
-                        : launch_stream_typed<__half, 8>(k_map16, v_map16, a, (int)ctas, stream);
-        case 16:
-            return bf16 ? launch_stream_typed<__nv_bfloat16, 16>(k_map16, v_map16, a, (int)ctas, stream)
-                        : launch_stream_typed<__half, 16>(k_map16, v_map16, a, (int)ctas, stream);
-        case 32:
-            return bf16 ? launch_stream_typed<__nv_bfloat16, 32>(k_map16, v_map16, a, (int)ctas, stream)
-                        : launch_stream_typed<__half, 32>(k_map16, v_map16, a, (int)ctas, stream);
-        case 64:
-            return bf16 ? launch_stream_typed<__nv_bfloat16, 64>(k_map16, v_map16, a, (int)ctas, stream)
-                        : launch_stream_typed<__half, 64>(k_map16, v_map16, a, (int)ctas, stream);
-        default:
-            return bf16 ? launch_stream_typed<__nv_bfloat16, 128>(k_map16, v_map16, a, (int)ctas, stream)
-                        : launch_stream_typed<__half, 128>(k_map16, v_map16, a, (int)ctas, stream);
-    }
+    return launch_stream<false>(k_map16, v_map16, a, dtype, block_size, stream);
+}
+
+cudaError_t launch_paged_decode_stream_fp8(const CUtensorMap& k_map8, const CUtensorMap& v_map8,
+                                           DecodeArgs a, pkv_dtype q_dtype, int block_size,
+                                           cudaStream_t stream) {
+    return launch_stream<true>(k_map8, v_map8, a, q_dtype, block_size, stream);
 }
 
 }  // namespace pkv

@@ -18,15 +18,23 @@ bool aligned(const void* p, uintptr_t bytes) {
     return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
 }
 
-bool valid_dtype(pkv_dtype d) { return d == PKV_FP16 || d == PKV_BF16; }
+bool valid_dtype(pkv_dtype d) { return d == PKV_FP16 || d == PKV_BF16 || d == PKV_FP8_E4M3; }
+bool valid_16bit(pkv_dtype d) { return d == PKV_FP16 || d == PKV_BF16; }
 
-// Geometry checks shared by every call.
+// Geometry checks shared by every call (any pool format).
 pkv_status check_cache(const pkv_cache_desc& c) {
     if (c.num_blocks <= 0 || c.num_kv_heads <= 0 || c.block_size <= 0 || c.head_dim <= 0 ||
         !valid_dtype(c.dtype))
         return PKV_ERR_INVALID_ARG;
-    if (c.head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;  // 16-byte rows
+    if ((c.head_dim * pkv::elem_bytes(c.dtype)) % 16 != 0) return PKV_ERR_UNSUPPORTED;  // 16-byte rows
     return PKV_OK;
+}
+
+// The calls whose q / k / v / out share the pools' 16-bit type.
+pkv_status check_cache_16bit(const pkv_cache_desc& c) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    return valid_16bit(c.dtype) ? PKV_OK : PKV_ERR_INVALID_ARG;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -44,21 +52,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A 4-D view of one pool, {head_dim, block_size, num_kv_heads, num_blocks}
-// (innermost first), tiled in boxes of {64, box_rows, 1, 1} with the
+// (innermost first), tiled in boxes of {128 bytes, box_rows, 1, 1} with the
 // 128-byte swizzle: one box is one half (64 columns) of box_rows token rows
-// of a (block, head) tile (box_rows = block_size, or 16 for streamed tiles).
+// of a (block, head) tile of a 16-bit pool, or a whole row of 128 codes of
+// an 8-bit pool (box_rows = block_size, or 16 for streamed tiles).
 bool encode_pool(CUtensorMap* map, const void* base, const pkv_cache_desc& c, int box_rows) {
     auto encode = tensor_map_encoder();
     if (encode == nullptr) return false;
-    const cuuint64_t row = static_cast<cuuint64_t>(c.head_dim) * 2;
+    const int eb = pkv::elem_bytes(c.dtype);
+    const cuuint64_t row = static_cast<cuuint64_t>(c.head_dim) * eb;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.head_dim), static_cast<cuuint64_t>(c.block_size),
                           static_cast<cuuint64_t>(c.num_kv_heads),
                           static_cast<cuuint64_t>(c.num_blocks)};
     cuuint64_t strides[3] = {row, row * c.block_size, row * c.block_size * c.num_kv_heads};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows), 1, 1};
     cuuint32_t elem[4] = {1, 1, 1, 1};
     const CUtensorMapDataType type =
-        c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        c.dtype == PKV_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+        : c.dtype == PKV_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     CUresult r = encode(map, type, 4, const_cast<void*>(base), dims, strides, box, elem,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -98,7 +110,7 @@ size_t workspace_for(int32_t num_seqs, int32_t num_q_heads, int32_t max_partitio
 
 extern "C" {
 
-int32_t pkv_abi_version(void) { return 100; }
+int32_t pkv_abi_version(void) { return 101; }
 
 const char* pkv_status_string(pkv_status status) {
     switch (status) {
@@ -114,7 +126,7 @@ const char* pkv_status_string(pkv_status status) {
 pkv_status pkv_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
                         int32_t num_tokens, void* k_cache, void* v_cache, pkv_cache_desc c,
                         int32_t* err_flag, void* stream) {
-    pkv_status st = check_cache(c);
+    pkv_status st = check_cache_16bit(c);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0) return PKV_OK;
@@ -155,7 +167,7 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
                                       float scale, int32_t partition_size, void* workspace,
                                       size_t workspace_bytes, void* out, int32_t* err_flag,
                                       void* stream) {
-    pkv_status st = check_cache(c);
+    pkv_status st = check_cache_16bit(c);
     if (st != PKV_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
         partition_size < 0 || !std::isfinite(scale))
@@ -220,6 +232,7 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
     a.max_partitions = max_parts;
     a.max_seq_len = max_seq_len;
     a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    a.v_scale = 1.f;
     cudaError_t e =
         streaming ? pkv::launch_paged_decode_stream(k_map, v_map, a, c.dtype, c.block_size,
                                                     static_cast<cudaStream_t>(stream))
@@ -238,7 +251,7 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc c,
     if (!k_cache || !v_cache || !src_dst_pairs) return PKV_ERR_INVALID_ARG;
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst_pairs, 8))
         return PKV_ERR_INVALID_ARG;
-    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
+    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * pkv::row_vectors(c);
     if ((vecs + 1023) / 1024 > 65535) return PKV_ERR_UNSUPPORTED;
     cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, c, src_dst_pairs, num_pairs,
                                             err_flag, static_cast<cudaStream_t>(stream));
@@ -251,7 +264,7 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
                                        const int32_t* seq_lens, int32_t max_seq_len,
                                        int32_t num_seqs, int32_t num_q_heads, pkv_cache_desc c,
                                        float scale, void* out, int32_t* err_flag, void* stream) {
-    pkv_status st = check_cache(c);
+    pkv_status st = check_cache_16bit(c);
     if (st != PKV_OK) return st;
     if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
         max_q_len < 0 || !std::isfinite(scale))
@@ -295,6 +308,86 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
     a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     cudaError_t e = pkv::launch_paged_prefill(k_map, v_map, a, c.dtype, c.block_size,
                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_kv_write_fp8(const void* k, const void* v, pkv_dtype kv_dtype,
+                            const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                            void* v_cache, pkv_cache_desc c, float k_scale, float v_scale,
+                            int32_t* err_flag, void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (c.dtype != PKV_FP8_E4M3 || !valid_16bit(kv_dtype) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::launch_kv_write_fp8(k, v, kv_dtype, slot_mapping, num_tokens, k_cache,
+                                             v_cache, c, k_scale, v_scale, err_flag,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_paged_decode_attention_fp8(const void* q, pkv_dtype q_dtype, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                          int32_t max_seq_len, int32_t num_seqs,
+                                          int32_t num_q_heads, pkv_cache_desc c, float scale,
+                                          float k_scale, float v_scale, void* workspace,
+                                          size_t workspace_bytes, void* out, int32_t* err_flag,
+                                          void* stream) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (c.dtype != PKV_FP8_E4M3 || !valid_16bit(q_dtype)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+        !std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale) ||
+        !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % c.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * c.block_size)
+        return PKV_ERR_INVALID_ARG;
+    const float scale_log2 = scale * k_scale * 1.4426950408889634f;  // log2(e)
+    if (!std::isfinite(scale_log2)) return PKV_ERR_INVALID_ARG;
+    const int32_t group = num_q_heads / c.num_kv_heads;
+    if (c.head_dim != kHeadDim || c.num_kv_heads > 65535 ||
+        !pkv::stream_supported(num_seqs > 0 ? num_seqs : 1, group, c.block_size))
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 8) || !aligned(out, 8) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    const size_t need = pkv::stream_workspace_bytes(num_seqs, num_q_heads, c.num_kv_heads);
+    if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+
+    CUtensorMap k_map, v_map;
+    const int box_rows = c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens;
+    if (!encode_pool(&k_map, k_cache, c, box_rows) || !encode_pool(&v_map, v_cache, c, box_rows))
+        return PKV_ERR_CUDA;
+    pkv::DecodeArgs a{};
+    a.q = q;
+    a.out = out;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.ws_acc = static_cast<float*>(workspace);  // laid out by the stream launcher
+    a.err = err_flag;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = c.num_kv_heads;
+    a.group = group;
+    a.num_blocks = c.num_blocks;
+    a.partition_size = 0;
+    a.max_partitions = 1;
+    a.max_seq_len = max_seq_len;
+    a.scale_log2 = scale_log2;
+    a.v_scale = v_scale;
+    cudaError_t e = pkv::launch_paged_decode_stream_fp8(k_map, v_map, a, q_dtype, c.block_size,
+                                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -347,7 +440,7 @@ pkv_status pkv_kv_write_layers(const void* const* k, const void* const* v,
                                const int64_t* slot_mapping, int32_t num_tokens,
                                void* const* k_caches, void* const* v_caches, int32_t num_layers,
                                pkv_cache_desc c, int32_t* err_flag, void* stream) {
-    pkv_status st = check_cache(c);
+    pkv_status st = check_cache_16bit(c);
     if (st != PKV_OK) return st;
     if (num_tokens < 0 || num_layers < 1 || num_layers > PKV_MAX_LAYERS) return PKV_ERR_INVALID_ARG;
     if (!k || !v || !k_caches || !v_caches) return PKV_ERR_INVALID_ARG;

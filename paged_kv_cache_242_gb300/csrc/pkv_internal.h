@@ -17,6 +17,10 @@ constexpr int kConsumerWarps = 4;    // warps that compute on staged K/V tiles
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kAutoPartition = 512;  // tokens per partition in automatic split mode
 
+// Bytes of one stored scalar of a pool, and 16-byte vectors per (token, head) row.
+inline int elem_bytes(pkv_dtype d) { return d == PKV_FP8_E4M3 ? 1 : 2; }
+inline int32_t row_vectors(const pkv_cache_desc& c) { return c.head_dim * elem_bytes(c.dtype) / 16; }
+
 // Launch `kernel` on `stream` with programmatic stream serialisation allowed
 // (the kernel waits for its prerequisites itself, see pkv_device.cuh).
 template <typename... KernelArgs, typename... Args>
@@ -76,9 +80,10 @@ struct DecodeArgs {
     int32_t partition_size;     // tokens per partition (multiple of block size)
     int32_t max_partitions;     // ceil(max_seq_len / partition_size), >= 1
     int32_t max_seq_len;
-    float scale_log2;           // softmax scale * log2(e)
+    float scale_log2;           // softmax scale * log2(e) (* k_scale for 8-bit pools)
     int32_t* ws_prefix;         // stream mode: [S + 1] tile prefix over sequences
     int32_t num_warps;          // stream mode: warps in the grid
+    float v_scale;              // 8-bit pools: value scale (1 otherwise)
 };
 
 #ifndef PKV_STREAM_WARPS
@@ -87,8 +92,12 @@ struct DecodeArgs {
 #ifndef PKV_STREAM_STAGES
 #define PKV_STREAM_STAGES 2
 #endif
+#ifndef PKV_STREAM_STAGES_FP8
+#define PKV_STREAM_STAGES_FP8 4
+#endif
 constexpr int kStreamWarps = PKV_STREAM_WARPS;    // warps per CTA of the streaming kernel
 constexpr int kStreamStages = PKV_STREAM_STAGES;  // 8 KiB stages per warp
+constexpr int kStreamStagesFp8 = PKV_STREAM_STAGES_FP8;  // 4 KiB stages per warp (8-bit pools)
 constexpr int kStreamMaxCtas = 160;     // cap of its grid (one CTA per SM)
 constexpr int kStreamMaxSeqs = 4096;    // sequences whose prefix fits shared memory
 constexpr int kTileTokens = 16;         // tokens per streamed tile
@@ -101,6 +110,11 @@ size_t stream_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads_or
 cudaError_t launch_paged_decode_stream(const CUtensorMap& k_map16, const CUtensorMap& v_map16,
                                        DecodeArgs args, pkv_dtype dtype, int block_size,
                                        cudaStream_t stream);
+// The same over 8-bit (E4M3) pools; q_dtype is the type of q and out, the
+// maps view the pools as bytes (one 128-byte box per 16 token rows).
+cudaError_t launch_paged_decode_stream_fp8(const CUtensorMap& k_map8, const CUtensorMap& v_map8,
+                                           DecodeArgs args, pkv_dtype q_dtype, int block_size,
+                                           cudaStream_t stream);
 
 // Launch the split (or single-pass, when max_partitions == 1) decode
 // kernel and, in split mode, the merge kernel.
@@ -133,6 +147,11 @@ cudaError_t launch_paged_prefill(const CUtensorMap& k_map16, const CUtensorMap& 
 cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
                             int32_t num_tokens, void* k_cache, void* v_cache,
                             const pkv_cache_desc& c, int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_kv_write_fp8(const void* k, const void* v, pkv_dtype kv_dtype,
+                                const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                                void* v_cache, const pkv_cache_desc& c, float k_scale,
+                                float v_scale, int32_t* err, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc& c,
                                const int64_t* pairs, int32_t num_pairs, int32_t* err,

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) kv_write_layers_kernel(
 }
 
 int64_t chunks_of(const pkv_cache_desc& c) {
-    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
+    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * row_vectors(c);
     return (vecs + kVecsPerCta - 1) / kVecsPerCta;
 }
 
@@ -145,7 +145,7 @@ cudaError_t launch_transfer_blocks(const void* src_k, const void* src_v, int32_t
                                    const pkv_cache_desc& c, const int64_t* pairs,
                                    int32_t num_pairs, int32_t* err, cudaStream_t stream) {
     if (num_pairs == 0) return cudaSuccess;
-    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
+    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * row_vectors(c);
     return launch_pdl(transfer_blocks_kernel,
                       dim3(static_cast<unsigned>(num_pairs), static_cast<unsigned>(chunks_of(c))),
                       dim3(kThreads), 0, stream, static_cast<const uint4*>(src_k),
@@ -163,7 +163,7 @@ cudaError_t launch_copy_blocks_layers(void* const* k_caches, void* const* v_cach
         caches.k[l] = static_cast<uint4*>(k_caches[l]);
         caches.v[l] = static_cast<uint4*>(v_caches[l]);
     }
-    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * c.head_dim / 8;
+    const int64_t vecs = static_cast<int64_t>(c.num_kv_heads) * c.block_size * row_vectors(c);
     return launch_pdl(copy_blocks_layers_kernel,
                       dim3(static_cast<unsigned>(num_pairs), static_cast<unsigned>(chunks_of(c)),
                            static_cast<unsigned>(num_layers)),

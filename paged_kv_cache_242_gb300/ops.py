@@ -15,7 +15,11 @@ import torch
 from . import _lib
 from ._lib import CacheDesc, PKVError
 
-_DTYPES = {torch.float16: _lib.PKV_FP16, torch.bfloat16: _lib.PKV_BF16}
+_DTYPES = {torch.float16: _lib.PKV_FP16, torch.bfloat16: _lib.PKV_BF16,
+           torch.uint8: _lib.PKV_FP8_E4M3}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPES[torch.float8_e4m3fn] = _lib.PKV_FP8_E4M3
+_16BIT = {torch.float16: _lib.PKV_FP16, torch.bfloat16: _lib.PKV_BF16}
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -182,6 +186,79 @@ def paged_prefill_attention(q: torch.Tensor, cu_seqlens_q: torch.Tensor, k_cache
     return out
 
 
+def _check_fp8_pools(k_cache: torch.Tensor, v_cache: torch.Tensor) -> CacheDesc:
+    _check_caches(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    _require(desc.dtype == _lib.PKV_FP8_E4M3,
+             "8-bit pools hold E4M3 codes as torch.uint8 (or torch.float8_e4m3fn)")
+    return desc
+
+
+def kv_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: float, v_scale: float,
+                 err_flag: Optional[torch.Tensor] = None) -> None:
+    """Store k, v [T, H_kv, d] (fp16 / bf16) as E4M3 codes of x / scale at ``slot_mapping``."""
+    desc = _check_fp8_pools(k_cache, v_cache)
+    T = int(slot_mapping.numel())
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and
+             slot_mapping.is_contiguous(), "slot_mapping must be a contiguous CUDA int64 tensor")
+    _require(k.shape == (T, desc.num_kv_heads, desc.head_dim) and v.shape == k.shape,
+             "k and v must be [num_tokens, num_kv_heads, head_dim]")
+    _require(k.dtype in _16BIT and v.dtype == k.dtype, "k and v must be float16 or bfloat16")
+    _require(k.is_contiguous() and v.is_contiguous() and k.is_cuda and v.is_cuda,
+             "k and v must be contiguous CUDA tensors")
+    lib = _lib.load()
+    _lib.check(lib.pkv_kv_write_fp8(_ptr(k), _ptr(v), _16BIT[k.dtype], _ptr(slot_mapping), T,
+                                    _ptr(k_cache), _ptr(v_cache), desc,
+                                    ctypes.c_float(float(k_scale)), ctypes.c_float(float(v_scale)),
+                                    _err_ptr(err_flag), _stream(k_cache.device)),
+               "pkv_kv_write_fp8")
+
+
+def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                               k_scale: float, v_scale: float, scale: Optional[float] = None,
+                               out: Optional[torch.Tensor] = None, *,
+                               max_seq_len: Optional[int] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_decode_attention over E4M3 pools read back as code * scale.
+
+    q [S, H_q, d] float16 / bfloat16 (the output's type); other arguments as
+    ``paged_decode_attention`` in automatic mode.
+    """
+    desc = _check_fp8_pools(k_cache, v_cache)
+    _require(q.dim() == 3 and q.shape[2] == desc.head_dim, "q must be [num_seqs, num_q_heads, d]")
+    _require(q.dtype in _16BIT and q.is_cuda and q.is_contiguous(),
+             "q must be a contiguous CUDA float16 / bfloat16 tensor")
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+             block_tables.shape[0] == S and block_tables.is_contiguous() and block_tables.is_cuda,
+             "block_tables must be a contiguous CUDA int32 [num_seqs, max_blocks] tensor")
+    _require(seq_lens.dtype == torch.int32 and seq_lens.numel() == S and seq_lens.is_cuda and
+             seq_lens.is_contiguous(), "seq_lens must be a contiguous CUDA int32 [num_seqs] tensor")
+    if scale is None:
+        scale = desc.head_dim ** -0.5
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if S > 0 else 0
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous() and out.is_cuda,
+             "out must match q")
+    if workspace is None:
+        need = decode_workspace_bytes(S, Hq, max_seq_len, desc.block_size, 0, desc.head_dim)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    _lib.check(lib.pkv_paged_decode_attention_fp8(
+        _ptr(q), _16BIT[q.dtype], _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(seq_lens), int(max_seq_len), S, Hq, desc,
+        ctypes.c_float(float(scale)), ctypes.c_float(float(k_scale)),
+        ctypes.c_float(float(v_scale)), _ptr(workspace), ws_bytes, _ptr(out),
+        _err_ptr(err_flag), _stream(q.device)), "pkv_paged_decode_attention_fp8")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor,
                 err_flag: Optional[torch.Tensor] = None) -> None:
     """Copy whole blocks src -> dst of both caches; pairs int64 [P, 2] on the device."""
@@ -283,4 +360,5 @@ def copy_blocks_layers(k_caches, v_caches, src_dst_pairs: torch.Tensor,
 
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
            "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
-           "copy_blocks_layers", "paged_prefill_attention"]
+           "copy_blocks_layers", "paged_prefill_attention", "kv_write_fp8",
+           "paged_decode_attention_fp8"]

@@ -48,7 +48,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE_TOO_SMALL"
-    assert lib.pkv_abi_version() == 100
+    assert lib.pkv_abi_version() == 101
 
 
 def test_partition_and_workspace_queries(lib):
@@ -144,6 +144,67 @@ def test_host_validation_without_launch(lib):
     assert lib.pkv_copy_blocks(fake, fake, _desc(), null, 3, null, null) == 1
     assert lib.pkv_copy_blocks(null, null, _desc(), null, 0, null, null) == 0
     assert lib.pkv_copy_blocks(fake, fake, _desc(), fake, -1, null, null) == 1
+
+
+def test_fp8_validation_without_launch(lib):
+    """The 8-bit pool calls, and 8-bit pools in the 16-bit calls, fail validation first."""
+    fake = ctypes.c_void_p(0x10000)
+    null = None
+    d8 = _desc(dtype=_lib.PKV_FP8_E4M3)
+    # the 16-bit calls take 16-bit pools only
+    assert lib.pkv_kv_write(fake, fake, fake, 1, fake, fake, d8, null, null) == 1
+    assert lib.pkv_paged_decode_attention(fake, fake, fake, fake, 4, fake, 64, 2, 32, d8,
+                                          ctypes.c_float(0.1), 0, null, 0, fake, null, null) == 1
+    assert lib.pkv_paged_prefill_attention(fake, fake, 4, fake, fake, fake, 4, fake, 64, 2, 32,
+                                           d8, ctypes.c_float(0.1), fake, null, null) == 1
+
+    def kw8(**kw):
+        a = dict(k=fake, v=fake, kvd=_lib.PKV_BF16, sm=fake, T=4, kc=fake, vc=fake, desc=d8,
+                 ks=0.5, vs=0.5)
+        a.update(kw)
+        return lib.pkv_kv_write_fp8(a["k"], a["v"], a["kvd"], a["sm"], a["T"], a["kc"], a["vc"],
+                                    a["desc"], ctypes.c_float(a["ks"]), ctypes.c_float(a["vs"]),
+                                    null, null)
+
+    assert kw8(T=0) == 0
+    assert kw8(k=null) == 1
+    assert kw8(kvd=_lib.PKV_FP8_E4M3) == 1  # new keys / values are 16-bit
+    assert kw8(desc=_desc()) == 1           # the pools must be 8-bit
+    assert kw8(ks=0.0) == 1 and kw8(vs=float("inf")) == 1 and kw8(ks=-1.0) == 1
+    assert kw8(desc=_desc(dtype=2, head_dim=8)) == 2  # 8-byte rows
+
+    def at8(**kw):
+        a = dict(q=fake, qd=_lib.PKV_BF16, kc=fake, vc=fake, bt=fake, mb=4, sl=fake, msl=64, S=2,
+                 Hq=32, desc=d8, scale=0.1, ks=0.5, vs=0.5, ws=null, wsb=0, out=fake)
+        a.update(kw)
+        return lib.pkv_paged_decode_attention_fp8(
+            a["q"], a["qd"], a["kc"], a["vc"], a["bt"], a["mb"], a["sl"], a["msl"], a["S"],
+            a["Hq"], a["desc"], ctypes.c_float(a["scale"]), ctypes.c_float(a["ks"]),
+            ctypes.c_float(a["vs"]), a["ws"], a["wsb"], a["out"], null, null)
+
+    assert at8(S=0) == 0
+    assert at8() == 3  # the streaming kernel needs its workspace
+    assert at8(desc=_desc()) == 1
+    assert at8(qd=_lib.PKV_FP8_E4M3) == 1
+    assert at8(ks=0.0) == 1 and at8(vs=float("nan")) == 1
+    assert at8(scale=1e30, ks=1e30) == 1  # the combined score factor overflows
+    assert at8(Hq=30) == 1
+    assert at8(msl=65) == 1
+    assert at8(Hq=8 * 17) == 2  # group of 17 query heads per KV head
+    assert at8(desc=_desc(dtype=2, head_dim=64)) == 2
+    assert at8(desc=_desc(dtype=2, block_size=24), msl=48) == 2
+    assert at8(S=5000, mb=4) == 2  # more sequences than the streaming kernel takes
+    assert at8(q=null, ws=fake, wsb=1 << 30) == 1
+    # block copies take 8-bit pools as they are
+    assert lib.pkv_copy_blocks(null, null, d8, null, 0, null, null) == 0
+    assert lib.pkv_copy_blocks(fake, fake, d8, null, 3, null, null) == 1
+    assert lib.pkv_swap_blocks(fake, fake, 4, fake, fake, 4, d8, fake, 0, null, null) == 0
+
+
+def test_workspace_query_covers_the_fp8_call(lib):
+    from paged_kv_cache_242_gb300 import ops  # noqa: F401  (binding loads)
+    for S, Hq, msl in ((1, 8, 1), (64, 32, 4096), (4096, 64, 100)):
+        assert lib.pkv_decode_workspace_bytes(S, Hq, 128, msl, 16, 0) > 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true",
                     help="also measure the tiny, OPT-13B-like and prefix-sharing workloads")
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="pool format of the timed step: 16-bit pools, or 8-bit E4M3 pools "
+                         "(quantised from the same values) with the 8-bit write and attention")
     ap.add_argument("--seed", type=int, default=244)
     return ap.parse_args()
 
@@ -76,9 +79,10 @@ def attention_bytes(step, kv_scalar_bytes: int = 2) -> int:
     return kv + qo + tables
 
 
-def kv_write_bytes(step) -> int:
+def kv_write_bytes(step, kv_scalar_bytes: int = 2) -> int:
+    """New 16-bit keys / values read, pool scalars written, slot mapping read."""
     T = int(step.slot_mapping.numel())
-    return 2 * (2 * T * step.num_kv_heads * step.head_dim * 2) + 8 * T
+    return 2 * T * step.num_kv_heads * step.head_dim * (2 + kv_scalar_bytes) + 8 * T
 
 
 def copy_bytes(step) -> int:
@@ -108,7 +112,7 @@ def kernel_source_digest() -> str:
     return h.hexdigest()
 
 
-def traffic_for():
+def traffic_for(kv: str = "bf16"):
     """DRAM bytes per launch from a committed ncu capture of these exact sources."""
     path = os.path.join(ROOT, "profiles", "decode_stream_traffic.json")
     try:
@@ -118,7 +122,8 @@ def traffic_for():
         return None
     if rec.get("source_sha256") != kernel_source_digest():
         return None
-    return rec.get("dram_bytes_per_launch_gqa_batch")
+    key = "dram_bytes_per_launch_gqa_batch" + ("" if kv == "bf16" else "_fp8")
+    return rec.get(key)
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -540,6 +545,20 @@ def run_pkv(args, rank, world, local_rank):
         "q": step.q, "k_new": step.k_new, "v_new": step.v_new, "slot_mapping": step.slot_mapping,
         "block_tables": step.block_tables, "seq_lens": step.seq_lens,
         "cow_pairs": step.cow_pairs, "k_cache": step.k_cache, "v_cache": step.v_cache}.items()}
+    fp8 = args.kv == "fp8"
+    if fp8:  # 8-bit pools holding the same values, quantised by the 8-bit write
+        nb, h, b, d = step.k_cache.shape
+        kc8 = torch.empty((nb, h, b, d), dtype=torch.uint8, device=device)
+        vc8 = torch.empty_like(kc8)
+        rows = [dev[k].permute(0, 2, 1, 3).reshape(nb * b, h, d).contiguous()
+                for k in ("k_cache", "v_cache")]
+        pkv.kv_write_fp8(rows[0], rows[1], torch.arange(nb * b, dtype=torch.int64, device=device),
+                         kc8, vc8, FP8_K_SCALE, FP8_V_SCALE)
+        del rows
+        dev["k_cache"], dev["v_cache"] = kc8, vc8
+        if args.partition_size:
+            raise SystemExit("--kv fp8 streams (automatic mode): no --partition-size")
+    kvb = 1 if fp8 else 2
     part = pkv.decode_partition_size(step.max_seq_len, step.block_size, args.partition_size)
     split = part < step.max_seq_len
     ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
@@ -550,18 +569,33 @@ def run_pkv(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(device)
     has_cow = step.cow_pairs.numel() > 0
 
+    def attend(q, block_tables, seq_lens):
+        if fp8:
+            pkv.paged_decode_attention_fp8(q, dev["k_cache"], dev["v_cache"], block_tables,
+                                           seq_lens, FP8_K_SCALE, FP8_V_SCALE, step.scale, out,
+                                           max_seq_len=step.max_seq_len, workspace=workspace,
+                                           err_flag=err)
+        else:
+            pkv.paged_decode_attention(q, dev["k_cache"], dev["v_cache"], block_tables, seq_lens,
+                                       step.num_kv_heads, step.scale, out,
+                                       max_seq_len=step.max_seq_len,
+                                       partition_size=args.partition_size, workspace=workspace,
+                                       err_flag=err)
+
+    def put(k_new, v_new, slot_mapping):
+        if fp8:
+            pkv.kv_write_fp8(k_new, v_new, slot_mapping, dev["k_cache"], dev["v_cache"],
+                             FP8_K_SCALE, FP8_V_SCALE, err_flag=err)
+        else:
+            pkv.kv_write(k_new, v_new, slot_mapping, dev["k_cache"], dev["v_cache"], err_flag=err)
+
     def attention():
-        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
-                                   dev["seq_lens"], step.num_kv_heads, step.scale, out,
-                                   max_seq_len=step.max_seq_len,
-                                   partition_size=args.partition_size, workspace=workspace,
-                                   err_flag=err)
+        attend(dev["q"], dev["block_tables"], dev["seq_lens"])
 
     def write():
         if has_cow:
             pkv.copy_blocks(dev["k_cache"], dev["v_cache"], dev["cow_pairs"], err_flag=err)
-        pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
-                     dev["v_cache"], err_flag=err)
+        put(dev["k_new"], dev["v_new"], dev["slot_mapping"])
 
     # kv_write, copy_blocks when pairs exist, the attention kernel, and the
     # merge kernel (always in automatic mode; with explicit partitions only
@@ -607,8 +641,8 @@ def run_pkv(args, rank, world, local_rank):
     assert int(err.item()) == 0, f"device error flag {int(err.item())}"
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K
-    a_bytes = attention_bytes(step)
-    step_bytes = a_bytes + kv_write_bytes(step) + copy_bytes(step)
+    a_bytes = attention_bytes(step, kvb)
+    step_bytes = a_bytes + kv_write_bytes(step, kvb) + copy_bytes(step) // (2 // kvb)
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
     tokens_per_s = world * step.num_seqs / (ms_per_step * 1e-3)
 
@@ -639,14 +673,8 @@ def run_pkv(args, rank, world, local_rank):
 
         def e2e_step():
             staged_dev.copy_(staged, non_blocking=True)
-            pkv.kv_write(inputs["k_new"], inputs["v_new"], inputs["slot_mapping"],
-                         dev["k_cache"], dev["v_cache"], err_flag=err)
-            pkv.paged_decode_attention(inputs["q"], dev["k_cache"], dev["v_cache"],
-                                       inputs["block_tables"], inputs["seq_lens"],
-                                       step.num_kv_heads, step.scale, out,
-                                       max_seq_len=step.max_seq_len,
-                                       partition_size=args.partition_size, workspace=workspace,
-                                       err_flag=err)
+            put(inputs["k_new"], inputs["v_new"], inputs["slot_mapping"])
+            attend(inputs["q"], inputs["block_tables"], inputs["seq_lens"])
             out_host.copy_(out, non_blocking=True)
             torch.cuda.current_stream(device).synchronize()
 
@@ -659,7 +687,7 @@ def run_pkv(args, rank, world, local_rank):
             e2e_step()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
         e2e_s = max_over_ranks(e2e_s, world, device)
-        e2e = {"value": round(world * (a_bytes + kv_write_bytes(step)) / e2e_s / 1e9, 2),
+        e2e = {"value": round(world * (a_bytes + kv_write_bytes(step, kvb)) / e2e_s / 1e9, 2),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_s * 1e3, 4), "steps": e2e_steps,
                "decode_tokens_per_s": round(world * step.num_seqs / e2e_s, 1)}
@@ -675,17 +703,18 @@ def run_pkv(args, rank, world, local_rank):
         return
     hbm, kind = measured_peaks()
     achieved = a_bytes / (attn_ms * 1e-3) / 1e9
-    roofline = {"kernel": "paged_decode_attention (streaming kernel + merge kernel)",
+    roofline = {"kernel": ("paged_decode_attention_fp8" if fp8 else "paged_decode_attention")
+                          + " (streaming kernel + merge kernel)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_kind": f"{kind} (burst copy)",
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                 "algorithmic_bytes_per_launch": a_bytes,
                 "avg_call_ms": round(attn_ms, 5),
-                "traffic": traffic_for(),
+                "traffic": traffic_for(args.kv),
                 "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the streaming "
                                 "kernel alone (the merge kernel reads its ~4 MB of partials from L2)"}
     cpu = None
-    if world == 1 and not args.no_cpu:
+    if world == 1 and not args.no_cpu and not fp8:
         rate, _, desc, threads = oracle_sample_rate(step, 10.0)
         cpu = {"kind": "oracle", "value": round(rate / 1e9, 4), "unit": UNIT, "cores": threads,
                "sample": desc}
@@ -693,7 +722,9 @@ def run_pkv(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(step, part),
+        "data": "synthetic", "config": dict(workload_config(step, part),
+                                            kv_format="E4M3 codes, one scale per pool" if fp8
+                                            else "bf16"),
         "decode_tokens_per_s": round(tokens_per_s, 1),
         "step_bytes": step_bytes, "gpu_launches": launches_per_step * K,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clock_info,

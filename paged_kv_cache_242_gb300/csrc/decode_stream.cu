@@ -1,5 +1,6 @@
 // Streaming paged decode attention: a persistent grid with one CTA of
-// kStreamWarps (7) warps per SM, each warp an independent TMA pipeline.
+// kStreamWarps (7) warps per SM (8 over 8-bit pools), each warp an
+// independent TMA pipeline.
 //
 // What it computes is the same as the partition kernel (decode_attention.cu):
 // for every sequence and query head, softmax(scale * q K^T) V over the
@@ -10,7 +11,7 @@
 //
 // Work split.  All (sequence, KV head) segments are cut into 16-token tiles
 // (a whole block at block size 16, a slice of one block at 32 / 64 / 128,
-// two blocks at 8) and laid end to end in
+// two blocks at 8; 32-token tiles over 8-bit pools) and laid end to end in
 // (sequence, head, tile) order.  Warp w of the grid takes the contiguous
 // range [w * per, (w + 1) * per) of that order, per = ceil(tiles / warps), so
 // every warp streams the same number of bytes and the grid finishes together
@@ -44,19 +45,21 @@ namespace {
 // (E4M3 codes): one 128-byte box per tile (4 KiB), twice the stages.
 template <bool kFp8>
 struct StreamLayout {
+    static constexpr int kWarps = kFp8 ? kStreamWarpsFp8 : kStreamWarps;
+    static constexpr int kThreads = kWarps * 32;
     static constexpr int kStages = kFp8 ? kStreamStagesFp8 : kStreamStages;
+    static constexpr int kTileTokens = kFp8 ? kTileTokensFp8 : pkv::kTileTokens;
     static constexpr int kTileBytes = kTileTokens * kHeadDim * (kFp8 ? 1 : 2);  // K or V
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRingBytes = kStreamWarps * kStages * kStageBytes;
+    static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 };
-constexpr int kHalf = kTileTokens * 128;  // one 128-byte-wide box of 16 rows
-constexpr int kThreads = kStreamWarps * 32;
+constexpr int kHalf = kTileTokens * 128;  // one 64-column box of 16 rows of a 16-bit pool
 
-template <int kStages>
+template <int kWarps, int kStages>
 struct alignas(8) StreamControl {
-    uint64_t full[kStreamWarps][kStages];
-    int32_t valid[kStreamWarps][kStages];
-    int32_t warp_total[kStreamWarps];
+    uint64_t full[kWarps][kStages];
+    int32_t valid[kWarps][kStages];
+    int32_t warp_total[kWarps];
 };
 
 // Position of one tile in the (sequence, head, tile) order.
@@ -99,16 +102,19 @@ __device__ __forceinline__ Cursor cursor_at(int64_t t, const int32_t* prefix, in
 }
 
 template <typename T, int BS, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(StreamLayout<kFp8>::kThreads, 1)
     paged_decode_stream_kernel(const __grid_constant__ CUtensorMap k_map,
                                const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
     using L = StreamLayout<kFp8>;
+    constexpr int kWarps = L::kWarps;
+    constexpr int kThreads = L::kThreads;
     constexpr int kStages = L::kStages;
     constexpr int kStageBytes = L::kStageBytes;
+    constexpr int kTT = L::kTileTokens;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    auto* ctl = reinterpret_cast<StreamControl<kStages>*>(ring + L::kRingBytes);
+    auto* ctl = reinterpret_cast<StreamControl<kWarps, kStages>*>(ring + L::kRingBytes);
     int32_t* prefix = reinterpret_cast<int32_t*>(ctl + 1);  // [S + 1]
     int32_t* lens = prefix + a.num_seqs + 1;                // [S]
 
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- prologue: tile-count prefix over the sequences ---------------------
     {
-        const int per_thread = (S + kThreads - 1) / kThreads;  // <= 16
+        const int per_thread = (S + kThreads - 1) / kThreads;  // <= 19 (S <= 4096)
         const int base = threadIdx.x * per_thread;
         int sum = 0;
         for (int k = 0; k < per_thread; ++k) {
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (idx < S) {
                 const int n = clamped_len(a, idx, blockIdx.x == 0);
                 lens[idx] = n;
-                sum += (n + kTileTokens - 1) / kTileTokens;
+                sum += (n + kTT - 1) / kTT;
             }
         }
         // block-wide exclusive scan of the per-thread sums
@@ -145,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 31) ctl->warp_total[warp] = incl;
         if (threadIdx.x == 0) {
-            for (int w = 0; w < kStreamWarps; ++w) {
+            for (int w = 0; w < kWarps; ++w) {
                 for (int st = 0; st < kStages; ++st) mbar_init(smem_addr(&ctl->full[w][st]), 1);
             }
             fence_barrier_init();
@@ -158,12 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = base + k;
             if (idx < S) {
                 prefix[idx] = run;
-                run += (lens[idx] + kTileTokens - 1) / kTileTokens;
+                run += (lens[idx] + kTT - 1) / kTT;
             }
         }
         if (threadIdx.x == kThreads - 1) {
             int total = 0;
-            for (int w = 0; w < kStreamWarps; ++w) total += ctl->warp_total[w];
+            for (int w = 0; w < kWarps; ++w) total += ctl->warp_total[w];
             prefix[S] = total;
         }
         __syncthreads();
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- this warp's share of the tiles --------------------------------------
     const int64_t total_tiles = static_cast<int64_t>(prefix[S]) * H;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + warp;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     const int64_t per = total_tiles > 0 ? (total_tiles + a.num_warps - 1) / a.num_warps : 1;
     const int64_t t0 = gw * per;
     const int64_t t1 = min(t0 + per, total_tiles);
@@ -193,12 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A tile is 16 token rows: rows of one block when BS >= 16, two whole
     // blocks of 8 rows each when BS == 8 (the 128-byte swizzle repeats every
     // 8 rows, so two 8-row boxes land exactly as one 16-row box would).
-    constexpr int kBlocksPerTile = BS < kTileTokens ? kTileTokens / BS : 1;
-    constexpr int kBoxRows = BS < kTileTokens ? BS : kTileTokens;
+    constexpr int kBlocksPerTile = BS < kTT ? kTT / BS : 1;
+    constexpr int kBoxRows = BS < kTT ? BS : kTT;
     auto issue = [&](int k) {
         issued = k + 1;
         const int st = k % kStages;
-        const int blk = (iss.i * kTileTokens) / BS;  // first block of the tile
+        const int blk = (iss.i * kTT) / BS;  // first block of the tile
         const int nblocks = (lens[iss.s] + BS - 1) / BS;
         if (iss.s != win_s || blk < win_base || blk + kBlocksPerTile > win_base + 32) {
             win_s = iss.s;
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
                 const uint32_t vt = kt + L::kTileBytes;
-                const int row = (iss.i * kTileTokens) % BS;  // 0 when BS <= 16
+                const int row = (iss.i * kTT) % BS;  // 0 when BS <= kTT
                 fence_proxy_async_shared();  // earlier generic reads of this stage
                 mbar_arrive_expect_tx(full, present * kBoxRows * 128 * (kFp8 ? 2 : 4));
 #pragma unroll
@@ -370,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ctl->valid[warp][st]) {
             const uint32_t kt = smem_addr(my_ring + st * kStageBytes);
-            const int nvalid = min(kTileTokens, lens[cur.s] - cur.i * kTileTokens);
+            const int nvalid = min(kTT, lens[cur.s] - cur.i * kTT);
             if constexpr (kFp8)
-                attend_tile_e4m3<true>(kt, kt + L::kTileBytes, nvalid, qa, o, m0, m1, l0, l1, sl0,
+                attend_tile_e4m3<kTT, kFp8SplitP>(kt, kt + L::kTileBytes, nvalid, qa, o, m0, m1, l0, l1, sl0,
                                        sl1, lane);
             else
-                attend_block<T, kTileTokens, true>(kt, kt + L::kTileBytes, nvalid, qa, o, m0, m1,
+                attend_block<T, kTT, true>(kt, kt + L::kTileBytes, nvalid, qa, o, m0, m1,
                                                    l0, l1, a.scale_log2, lane);
         }
         __syncwarp();
@@ -470,7 +476,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
 
 template <bool kFp8>
 constexpr size_t stream_smem_bytes(int num_seqs) {
-    return 1024 + StreamLayout<kFp8>::kRingBytes + sizeof(StreamControl<StreamLayout<kFp8>::kStages>) +
+    return 1024 + StreamLayout<kFp8>::kRingBytes +
+           sizeof(StreamControl<StreamLayout<kFp8>::kWarps, StreamLayout<kFp8>::kStages>) +
            (2 * static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t);
 }
 
@@ -481,7 +488,8 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
     auto kernel = paged_decode_stream_kernel<T, BS, kFp8>;
     cudaError_t err = ensure_smem_limit<paged_decode_stream_kernel<T, BS, kFp8>>(smem);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(kernel, dim3(ctas), dim3(kThreads), smem, stream, k_map, v_map, a);
+    err = launch_pdl(kernel, dim3(ctas), dim3(StreamLayout<kFp8>::kThreads), smem, stream, k_map,
+                     v_map, a);
     if (err != cudaSuccess) return err;
     const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.group;
     const int64_t blocks = (items + kMergeWarps - 1) / kMergeWarps;
@@ -513,12 +521,14 @@ cudaError_t launch_stream(const CUtensorMap& k_map, const CUtensorMap& v_map, De
     if (err != cudaSuccess) return err;
     // enough CTAs for ~16 tiles per warp, at most one per SM
     const int64_t max_tiles = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
-                              ((a.max_seq_len + kTileTokens - 1) / kTileTokens);
-    int64_t ctas = (max_tiles + kStreamWarps * 16 - 1) / (kStreamWarps * 16);
+                              ((a.max_seq_len + StreamLayout<kFp8>::kTileTokens - 1) /
+                               StreamLayout<kFp8>::kTileTokens);
+    constexpr int kWarps = StreamLayout<kFp8>::kWarps;
+    int64_t ctas = (max_tiles + kWarps * 16 - 1) / (kWarps * 16);
     const int cap = sms < kStreamMaxCtas ? sms : kStreamMaxCtas;
     if (ctas > cap) ctas = cap;
     if (ctas < 1) ctas = 1;
-    a.num_warps = static_cast<int32_t>(ctas) * kStreamWarps;
+    a.num_warps = static_cast<int32_t>(ctas) * kWarps;
     // workspace layout: acc [rows][128], m [rows], l [rows], prefix [S + 1]
     const size_t rows = (static_cast<size_t>(a.num_warps) +
                          static_cast<size_t>(a.num_seqs) * a.num_kv_heads) * a.group;
@@ -544,7 +554,7 @@ bool stream_supported(int num_seqs, int group, int block_size) {
 // partial ids are (warp + segment) < warps + S * H_kv.  Without H_kv the
 // group is bounded by min(16, H_q).
 size_t stream_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads_or_0) {
-    const size_t warps = static_cast<size_t>(kStreamMaxCtas) * kStreamWarps;
+    const size_t warps = static_cast<size_t>(kStreamMaxCtas) * kStreamMaxWarps;
     size_t rows;
     if (num_kv_heads_or_0 > 0) {
         const size_t g = static_cast<size_t>(num_q_heads / num_kv_heads_or_0);

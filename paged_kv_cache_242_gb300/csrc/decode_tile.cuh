@@ -85,6 +85,7 @@ __device__ __forceinline__ void attend_block(uint32_t k_tile, uint32_t v_tile, i
     const float base0 = mn0 == -INFINITY ? 0.f : mn0;
     const float base1 = mn1 == -INFINITY ? 0.f : mn1;
     const float alpha0 = ex2(m0 - base0), alpha1 = ex2(m1 - base1);
+    const bool rescale = mn0 != m0 || mn1 != m1;
     m0 = mn0;
     m1 = mn1;
     float ps0 = 0.f, ps1 = 0.f;
@@ -99,12 +100,14 @@ __device__ __forceinline__ void attend_block(uint32_t k_tile, uint32_t v_tile, i
     }
     l0 = l0 * alpha0 + ps0;
     l1 = l1 * alpha1 + ps1;
+    if (__any_sync(0xffffffffu, rescale)) {  // some row's running maximum moved
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-        o[nd][0] *= alpha0;
-        o[nd][1] *= alpha0;
-        o[nd][2] *= alpha1;
-        o[nd][3] *= alpha1;
+        for (int nd = 0; nd < 16; ++nd) {
+            o[nd][0] *= alpha0;
+            o[nd][1] *= alpha0;
+            o[nd][2] *= alpha1;
+            o[nd][3] *= alpha1;
+        }
     }
 
     // ---- P as the A operand (accumulator layout == A-fragment layout) -----
@@ -181,8 +184,8 @@ __device__ __forceinline__ void load_q_fragments(uint32_t (&qa)[8][4], const T* 
 }
 
 // ---- 8-bit (E4M3) pools ------------------------------------------------------
-// A streamed tile is 16 token rows of 128 one-byte codes (one 128-byte TMA
-// box, 128-byte swizzle: the 16-byte chunk c of row t sits at chunk
+// A streamed tile is 16 or 32 token rows of 128 one-byte codes (128-byte TMA
+// boxes, 128-byte swizzle: the 16-byte chunk c of row t sits at chunk
 // c ^ (t & 7)).  Codes are widened to binary16 in registers, which is exact
 // (every E4M3 value is a binary16 value), and multiplied with binary16 query
 // fragments by mma.sync m16n8k16; the pool scales are applied to the fp32
@@ -202,51 +205,55 @@ __device__ __forceinline__ void load_q_fragments(uint32_t (&qa)[8][4], const T* 
 // holds dims 16 c + 2 n + p, and lane quad's accumulators cover the four
 // consecutive dims 16 c + 4 quad .. + 3.
 
-// Four codes (bytes 0..3) -> binary16 pairs (bytes 0, 1) and (bytes 2, 3).
+// Four codes (bytes 0..3) -> binary16 pairs (bytes 0, 1) and (bytes 2, 3),
+// lower byte to the lower half (cvt.rn.f16x2.e4m3x2, exact).
 __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
-    const __half2_raw a =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xffffu), __NV_E4M3);
-    const __half2_raw b =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x >> 16), __NV_E4M3);
-    lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-    hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
-// One 16-token tile of E4M3 codes.  sl0 / sl1: score factors (log2 units) of
-// this lane's two rows.
-template <bool kSplitP>
+// One tile of kTokens (16 or 32) token rows of E4M3 codes.  sl0 / sl1: score
+// factors (log2 units) of this lane's two rows.
+template <int kTokens, bool kSplitP>
 __device__ __forceinline__ void attend_tile_e4m3(uint32_t k_tile, uint32_t v_tile, int nvalid,
                                                  const uint32_t (&qa)[8][4], float (&o)[16][4],
                                                  float& m0, float& m1, float& l0, float& l1,
                                                  float sl0, float sl1, int lane) {
     using M = Mma<__half>;
+    constexpr int NT = kTokens / 8;   // n-tiles of 8 tokens
+    constexpr int KK = kTokens / 16;  // k-steps of 16 tokens for P V
     const int mi = lane >> 3;
     const int r = lane & 7;
     const int quad = lane & 3;
-    const int token = (mi & 1) * 8 + r;  // row this lane addresses for ldmatrix
+    const int row = (mi & 1) * 8 + r;  // row (within 16) this lane addresses for ldmatrix
 
     // ---- S = Q K^T: each ldmatrix.x4 covers 2 n-tiles x 2 k-steps -----------
-    float sc[2][4];
+    float sc[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-    for (int kp = 0; kp < 4; ++kp) {
-        const int chunk = 2 * kp + (mi >> 1);
-        uint32_t d[4];
-        ldsm_x4(k_tile + token * 128 + ((chunk ^ r) << 4), d[0], d[1], d[2], d[3]);
-        // d[j]: n-tile j & 1, k-step 2 kp + (j >> 1)
+    for (int th = 0; th < KK; ++th) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16x2(d[j], b0, b1);
-            M::run(sc[j & 1], qa[2 * kp + (j >> 1)], b0, b1);
+        for (int kp = 0; kp < 4; ++kp) {
+            const int chunk = 2 * kp + (mi >> 1);
+            uint32_t d[4];
+            ldsm_x4(k_tile + (th * 16 + row) * 128 + ((chunk ^ r) << 4), d[0], d[1], d[2], d[3]);
+            // d[j]: n-tile 2 th + (j & 1), k-step 2 kp + (j >> 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t b0, b1;
+                e4m3x4_to_f16x2(d[j], b0, b1);
+                M::run(sc[2 * th + (j & 1)], qa[2 * kp + (j >> 1)], b0, b1);
+            }
         }
     }
 
     // ---- mask the unfilled tail, online softmax (Eq. 4) ------------------------
     float bm0 = -INFINITY, bm1 = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int col = nt * 8 + quad * 2 + (e & 1);
@@ -264,11 +271,12 @@ __device__ __forceinline__ void attend_tile_e4m3(uint32_t k_tile, uint32_t v_til
     const float base0 = mn0 == -INFINITY ? 0.f : mn0;
     const float base1 = mn1 == -INFINITY ? 0.f : mn1;
     const float alpha0 = ex2(m0 - base0), alpha1 = ex2(m1 - base1);
+    const bool rescale = mn0 != m0 || mn1 != m1;
     m0 = mn0;
     m1 = mn1;
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
         sc[nt][0] = ex2(sc[nt][0] - base0);
         sc[nt][1] = ex2(sc[nt][1] - base0);
         sc[nt][2] = ex2(sc[nt][2] - base1);
@@ -278,56 +286,67 @@ __device__ __forceinline__ void attend_tile_e4m3(uint32_t k_tile, uint32_t v_til
     }
     l0 = l0 * alpha0 + ps0;
     l1 = l1 * alpha1 + ps1;
+    if (__any_sync(0xffffffffu, rescale)) {  // some row's running maximum moved
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-        o[nd][0] *= alpha0;
-        o[nd][1] *= alpha0;
-        o[nd][2] *= alpha1;
-        o[nd][3] *= alpha1;
+        for (int nd = 0; nd < 16; ++nd) {
+            o[nd][0] *= alpha0;
+            o[nd][1] *= alpha0;
+            o[nd][2] *= alpha1;
+            o[nd][3] *= alpha1;
+        }
     }
 
     // ---- P (binary16, optionally split into high and low parts) -------------
-    uint32_t pa[4], pl[4];
+    uint32_t pa[KK][4], pl[KK][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int nt = e >> 1;
-        const int c = (e & 1) * 2;
-        pa[e] = M::pack(sc[nt][c], sc[nt][c + 1]);
-        if (kSplitP) {
-            const float2 hi = M::unpack(pa[e]);
-            pl[e] = M::pack(sc[nt][c] - hi.x, sc[nt][c + 1] - hi.y);
+    for (int kk = 0; kk < KK; ++kk) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int nt = 2 * kk + (e >> 1);
+            const int c = (e & 1) * 2;
+            pa[kk][e] = M::pack(sc[nt][c], sc[nt][c + 1]);
+            if (kSplitP) {
+                const float2 hi = M::unpack(pa[kk][e]);
+                pl[kk][e] = M::pack(sc[nt][c] - hi.x, sc[nt][c + 1] - hi.y);
+            }
         }
     }
 
     // ---- O += P V -----------------------------------------------------------------
-    const bool partial = nvalid < kTileTokens;
-    const int t0 = quad * 2;
-    const uint32_t keep0 = ((t0 < nvalid) ? 0x0000ffffu : 0u) | ((t0 + 1 < nvalid) ? 0xffff0000u : 0u);
-    const uint32_t keep1 = ((t0 + 8 < nvalid) ? 0x0000ffffu : 0u) | ((t0 + 9 < nvalid) ? 0xffff0000u : 0u);
+    const bool partial = nvalid < kTokens;
 #pragma unroll
-    for (int cp = 0; cp < 4; ++cp) {
-        const int chunk = 2 * cp + (mi >> 1);
-        uint32_t x[4];
-        ldsm_x4_trans(v_tile + token * 128 + ((chunk ^ r) << 4), x[0], x[1], x[2], x[3]);
-        // x[j]: tokens 8 (j & 1) .. + 7, chunk 2 cp + (j >> 1); bytes
-        // [tok 2quad: dim 2n, dim 2n+1 | tok 2quad+1: dim 2n, dim 2n+1]
+    for (int kk = 0; kk < KK; ++kk) {
+        const int t0 = kk * 16 + quad * 2;
+        const uint32_t keep0 =
+            ((t0 < nvalid) ? 0x0000ffffu : 0u) | ((t0 + 1 < nvalid) ? 0xffff0000u : 0u);
+        const uint32_t keep1 =
+            ((t0 + 8 < nvalid) ? 0x0000ffffu : 0u) | ((t0 + 9 < nvalid) ? 0xffff0000u : 0u);
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-            uint32_t even0, odd0, even1, odd1;
-            e4m3x4_to_f16x2(__byte_perm(x[2 * hc], 0, 0x3120), even0, odd0);
-            e4m3x4_to_f16x2(__byte_perm(x[2 * hc + 1], 0, 0x3120), even1, odd1);
-            if (partial) {  // unfilled rows may hold any codes (NaN too): zero them
-                even0 &= keep0;
-                odd0 &= keep0;
-                even1 &= keep1;
-                odd1 &= keep1;
-            }
-            const int ch = 2 * cp + hc;
-            M::run(o[2 * ch], pa, even0, even1);
-            M::run(o[2 * ch + 1], pa, odd0, odd1);
-            if (kSplitP) {
-                M::run(o[2 * ch], pl, even0, even1);
-                M::run(o[2 * ch + 1], pl, odd0, odd1);
+        for (int cp = 0; cp < 4; ++cp) {
+            const int chunk = 2 * cp + (mi >> 1);
+            uint32_t x[4];
+            ldsm_x4_trans(v_tile + (kk * 16 + row) * 128 + ((chunk ^ r) << 4), x[0], x[1], x[2],
+                          x[3]);
+            // x[j]: tokens 16 kk + 8 (j & 1) .. + 7, chunk 2 cp + (j >> 1); bytes
+            // [tok 2quad: dim 2n, dim 2n+1 | tok 2quad+1: dim 2n, dim 2n+1]
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                uint32_t even0, odd0, even1, odd1;
+                e4m3x4_to_f16x2(__byte_perm(x[2 * hc], 0, 0x3120), even0, odd0);
+                e4m3x4_to_f16x2(__byte_perm(x[2 * hc + 1], 0, 0x3120), even1, odd1);
+                if (partial) {  // unfilled rows may hold any codes (NaN too): zero them
+                    even0 &= keep0;
+                    odd0 &= keep0;
+                    even1 &= keep1;
+                    odd1 &= keep1;
+                }
+                const int ch = 2 * cp + hc;
+                M::run(o[2 * ch], pa[kk], even0, even1);
+                M::run(o[2 * ch + 1], pa[kk], odd0, odd1);
+                if (kSplitP) {
+                    M::run(o[2 * ch], pl[kk], even0, even1);
+                    M::run(o[2 * ch + 1], pl[kk], odd0, odd1);
+                }
             }
         }
     }

@@ -365,7 +365,7 @@ pkv_status pkv_paged_decode_attention_fp8(const void* q, pkv_dtype q_dtype, cons
     if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
 
     CUtensorMap k_map, v_map;
-    const int box_rows = c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens;
+    const int box_rows = c.block_size < pkv::kTileTokensFp8 ? c.block_size : pkv::kTileTokensFp8;
     if (!encode_pool(&k_map, k_cache, c, box_rows) || !encode_pool(&v_map, v_cache, c, box_rows))
         return PKV_ERR_CUDA;
     pkv::DecodeArgs a{};

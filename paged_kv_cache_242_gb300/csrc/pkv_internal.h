@@ -92,15 +92,31 @@ struct DecodeArgs {
 #ifndef PKV_STREAM_STAGES
 #define PKV_STREAM_STAGES 2
 #endif
+#ifndef PKV_STREAM_WARPS_FP8
+#define PKV_STREAM_WARPS_FP8 8
+#endif
 #ifndef PKV_STREAM_STAGES_FP8
-#define PKV_STREAM_STAGES_FP8 4
+#define PKV_STREAM_STAGES_FP8 2
+#endif
+#ifndef PKV_TILE_TOKENS_FP8
+#define PKV_TILE_TOKENS_FP8 32
+#endif
+#ifndef PKV_FP8_SPLIT_P
+#define PKV_FP8_SPLIT_P 0
 #endif
 constexpr int kStreamWarps = PKV_STREAM_WARPS;    // warps per CTA of the streaming kernel
 constexpr int kStreamStages = PKV_STREAM_STAGES;  // 8 KiB stages per warp
-constexpr int kStreamStagesFp8 = PKV_STREAM_STAGES_FP8;  // 4 KiB stages per warp (8-bit pools)
+// Over 8-bit pools: warps per CTA, tokens per streamed tile, stages per warp
+// (tile tokens x 256 bytes each), and whether P is split into two binary16
+// parts (binary16 P already carries 11 bits).
+constexpr int kStreamWarpsFp8 = PKV_STREAM_WARPS_FP8;
+constexpr int kTileTokensFp8 = PKV_TILE_TOKENS_FP8;
+constexpr int kStreamStagesFp8 = PKV_STREAM_STAGES_FP8;
+constexpr bool kFp8SplitP = PKV_FP8_SPLIT_P != 0;
+constexpr int kStreamMaxWarps = kStreamWarps > kStreamWarpsFp8 ? kStreamWarps : kStreamWarpsFp8;
 constexpr int kStreamMaxCtas = 160;     // cap of its grid (one CTA per SM)
 constexpr int kStreamMaxSeqs = 4096;    // sequences whose prefix fits shared memory
-constexpr int kTileTokens = 16;         // tokens per streamed tile
+constexpr int kTileTokens = 16;         // tokens per streamed tile (16-bit pools)
 
 // Streaming mode: every warp of a persistent grid takes an equal share of
 // all 16-token tiles in (sequence, KV head, tile) order; shares that cut a

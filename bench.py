@@ -100,7 +100,8 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-TRAFFIC_SOURCES = ("decode_stream.cu", "decode_tile.cuh", "pkv_device.cuh", "pkv_internal.h")
+TRAFFIC_SOURCES = ("decode_stream.cuh", "decode_policy.cuh", "decode_tile.cuh", "decode_stream.cu",
+                   "decode_stream_fp8.cu", "pkv_device.cuh", "pkv_internal.h")
 
 
 def kernel_source_digest() -> str:

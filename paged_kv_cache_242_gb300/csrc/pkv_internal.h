@@ -95,6 +95,9 @@ struct DecodeArgs {
 #ifndef PKV_STREAM_WARPS_FP8
 #define PKV_STREAM_WARPS_FP8 8
 #endif
+#ifndef PKV_STREAM_WARPS_FP8_COLS
+#define PKV_STREAM_WARPS_FP8_COLS 8
+#endif
 #ifndef PKV_STREAM_STAGES_FP8
 #define PKV_STREAM_STAGES_FP8 2
 #endif
@@ -109,11 +112,15 @@ constexpr int kStreamStages = PKV_STREAM_STAGES;  // 8 KiB stages per warp
 // Over 8-bit pools: warps per CTA, tokens per streamed tile, stages per warp
 // (tile tokens x 256 bytes each), and whether P is split into two binary16
 // parts (binary16 P already carries 11 bits).
-constexpr int kStreamWarpsFp8 = PKV_STREAM_WARPS_FP8;
+constexpr int kStreamWarpsFp8 = PKV_STREAM_WARPS_FP8;          // groups of 9..16 heads
+constexpr int kStreamWarpsFp8Cols = PKV_STREAM_WARPS_FP8_COLS;  // groups of up to 8 heads
 constexpr int kTileTokensFp8 = PKV_TILE_TOKENS_FP8;
 constexpr int kStreamStagesFp8 = PKV_STREAM_STAGES_FP8;
 constexpr bool kFp8SplitP = PKV_FP8_SPLIT_P != 0;
-constexpr int kStreamMaxWarps = kStreamWarps > kStreamWarpsFp8 ? kStreamWarps : kStreamWarpsFp8;
+constexpr int kStreamMaxWarps =
+    (kStreamWarps > kStreamWarpsFp8 ? kStreamWarps : kStreamWarpsFp8) > kStreamWarpsFp8Cols
+        ? (kStreamWarps > kStreamWarpsFp8 ? kStreamWarps : kStreamWarpsFp8)
+        : kStreamWarpsFp8Cols;
 constexpr int kStreamMaxCtas = 160;     // cap of its grid (one CTA per SM)
 constexpr int kStreamMaxSeqs = 4096;    // sequences whose prefix fits shared memory
 constexpr int kTileTokens = 16;         // tokens per streamed tile (16-bit pools)

@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true",
                     help="also measure the tiny, OPT-13B-like and prefix-sharing workloads")
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="time only the causal paged prefill of the prefill batch (one JSON line)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="pool format of the timed step: 16-bit pools, or 8-bit E4M3 pools "
                          "(quantised from the same values) with the 8-bit write and attention")
@@ -750,6 +752,18 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.only == "prefill":
+            import paged_kv_cache_242_gb300 as pkv
+            from paged_kv_cache_242_gb300 import workloads as W
+
+            pkv._lib.load()
+            device = torch.device("cuda", local_rank)
+            torch.cuda.set_device(device)
+            rec = measure_prefill(pkv, W, device)
+            if rank == 0:
+                print(json.dumps(dict(metric="causal paged prefill useful TFLOP/s",
+                                      value=rec["useful_tflops"], unit="TFLOP/s", **rec)),
+                      flush=True)
         else:
             run_pkv(args, rank, world, local_rank)
     finally:

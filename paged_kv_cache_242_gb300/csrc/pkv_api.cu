@@ -286,8 +286,11 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
     const int64_t row_tiles =
         (static_cast<int64_t>(max_q_len) * (num_q_heads / c.num_kv_heads) + 15) / 16;
     if (row_tiles > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    const bool tensor_cores = pkv::prefill_tc_supported(num_q_heads / c.num_kv_heads);
     CUtensorMap k_map, v_map;
-    const int box_rows = c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens;
+    const int box_rows =
+        tensor_cores ? pkv::prefill_tc_box_rows(c.block_size)
+                     : (c.block_size < pkv::kTileTokens ? c.block_size : pkv::kTileTokens);
     if (!encode_pool(&k_map, k_cache, c, box_rows) || !encode_pool(&v_map, v_cache, c, box_rows))
         return PKV_ERR_CUDA;
     pkv::PrefillArgs a{};
@@ -306,8 +309,12 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
     a.max_seq_len = max_seq_len;
     a.max_q_len = max_q_len;
     a.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-    cudaError_t e = pkv::launch_paged_prefill(k_map, v_map, a, c.dtype, c.block_size,
-                                              static_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        tensor_cores
+            ? pkv::launch_paged_prefill_tc(k_map, v_map, a, c.dtype, c.block_size,
+                                           static_cast<cudaStream_t>(stream))
+            : pkv::launch_paged_prefill(k_map, v_map, a, c.dtype, c.block_size,
+                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

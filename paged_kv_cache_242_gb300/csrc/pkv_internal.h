@@ -167,6 +167,14 @@ cudaError_t launch_paged_prefill(const CUtensorMap& k_map16, const CUtensorMap& 
                                  const PrefillArgs& args, pkv_dtype dtype, int block_size,
                                  cudaStream_t stream);
 
+// The tcgen05 prefill kernel (groups dividing 128); its pool maps use boxes
+// of prefill_tc_box_rows(block_size) token rows.
+bool prefill_tc_supported(int group);
+int prefill_tc_box_rows(int block_size);
+cudaError_t launch_paged_prefill_tc(const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                    const PrefillArgs& args, pkv_dtype dtype, int block_size,
+                                    cudaStream_t stream);
+
 cudaError_t launch_kv_write(const void* k, const void* v, const int64_t* slot_mapping,
                             int32_t num_tokens, void* k_cache, void* v_cache,
                             const pkv_cache_desc& c, int32_t* err, cudaStream_t stream);

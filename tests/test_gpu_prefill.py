@@ -42,9 +42,10 @@ def _reference(step):
 
 
 @pytest.mark.parametrize("B", [8, 16, 32, 128])
-@pytest.mark.parametrize("heads", [(8, 8), (32, 8), (16, 2)])
+@pytest.mark.parametrize("heads", [(8, 8), (32, 8), (16, 2), (24, 8), (20, 4)])
 def test_prefill_ragged(B, heads):
-    """Contexts and prompt lengths around 16-token sub-tiles and 64-key tiles."""
+    """Contexts and prompt lengths around 16-token sub-tiles and 64- / 128-key tiles; groups of
+    1, 4 and 8 query heads run on the tensor-core kernel, groups of 3 and 5 on the warp-MMA one."""
     H_q, H_kv = heads
     ctx = [0, 5, 16, 100, 0, 37]
     ql = [1, 7, 16, 65, 200, 64]
@@ -95,3 +96,23 @@ def test_prefill_bad_lengths_set_flag():
     torch.cuda.synchronize()
     assert int(err.item()) & _lib.DEVERR_BAD_SEQ_LEN
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("B", [16, 128])
+def test_prefill_nan_in_unfilled_slots(B):
+    """NaN in every slot no sequence fills must not reach any output (the last key tile
+    of a sequence reaches past its end)."""
+    step = W.build_prefill_step("nan", [3, 0, 130], [40, 77, 5], 32, 8, B, "bfloat16", seed=11)
+    filled = torch.zeros(step.k_cache.shape[0] * B, dtype=torch.bool)
+    for s, n in enumerate(step.seq_lens.tolist()):
+        for t in range(n):
+            filled[int(step.block_tables[s, t // B]) * B + t % B] = True
+    nb, hkv, _, d = step.k_cache.shape
+    for pool in (step.k_cache, step.v_cache):
+        rows = pool.permute(0, 2, 1, 3).reshape(nb * B, hkv, d)
+        rows[~filled] = float("nan")
+        pool.copy_(rows.reshape(nb, B, hkv, d).permute(0, 2, 1, 3))
+    out, _ = _run(step)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert_attention_close(out, _reference(step), f"prefill NaN-filled B={B}")

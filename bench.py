@@ -45,6 +45,8 @@ METRIC = "paged decode attention achieved HBM GB/s (% of GB300 peak) and decode 
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
+SINGLE_WORKLOADS = ("tiny", "opt13b_like", "long_context", "long_context_fp8", "prefix_sharing",
+                    "prefix_sharing_cow")
 
 
 def parse_args():
@@ -59,8 +61,10 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true",
                     help="also measure the tiny, OPT-13B-like and prefix-sharing workloads")
     ap.add_argument("--partition-size", type=int, default=0)
-    ap.add_argument("--only", choices=["prefill"], default=None,
-                    help="time only the causal paged prefill of the prefill batch (one JSON line)")
+    ap.add_argument("--only", choices=["prefill"] + sorted(SINGLE_WORKLOADS), default=None,
+                    help="time one workload alone and print one JSON line: the causal paged "
+                         "prefill of the prefill batch, or the decode attention of one of the "
+                         "other workloads (used for per-workload profiles)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="pool format of the timed step: 16-bit pools, or 8-bit E4M3 pools "
                          "(quantised from the same values) with the 8-bit write and attention")
@@ -274,19 +278,8 @@ def workload_config(step, partition=None):
     return cfg
 
 
-def time_attention_only(pkv, step, dev, part, reps=200, warmup=10):
-    """Average device time of one paged_decode_attention call (CUDA events)."""
-    ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
-                                          step.block_size, part)
-    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev["q"].device)
-    out = torch.empty_like(dev["q"])
-
-    def call():
-        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
-                                   dev["seq_lens"], step.num_kv_heads, step.scale, out,
-                                   max_seq_len=step.max_seq_len, partition_size=part,
-                                   workspace=ws)
-
+def time_calls(call, reps=200, warmup=10):
+    """Average time of one call issued back to back from Python (CUDA events)."""
     for _ in range(warmup):
         call()
     stream = torch.cuda.current_stream()
@@ -300,16 +293,88 @@ def time_attention_only(pkv, step, dev, part, reps=200, warmup=10):
     return e0.elapsed_time(e1) / reps
 
 
+L2_FLUSH_BYTES = 512 << 20  # written between calls whose inputs could stay in the 129 MB L2
+
+
+def time_calls_graph(call, per_graph=20, replays=10, flush=False):
+    """Average device time of one call replayed from a CUDA graph of `per_graph`
+    calls: no host launch cost, as a serving loop that captures its decode
+    step would issue it (median over replays, CUDA events).  With `flush`,
+    every call follows a 512 MiB write that evicts L2, and the time of a
+    graph of the writes alone is subtracted."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush else None
+
+    def build(with_call):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                if scratch is not None:
+                    scratch.fill_(1)
+                if with_call:
+                    call()
+        graph.replay()
+        torch.cuda.synchronize()
+        return graph
+
+    def median_ms(graph):
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(replays):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / per_graph)
+        times.sort()
+        return times[len(times) // 2]
+
+    ms = median_ms(build(True))
+    if scratch is not None:
+        ms -= median_ms(build(False))
+    return ms
+
+
+def time_attention_only(pkv, step, dev, part, reps=200, warmup=10, graph=False):
+    """Average device time of one paged_decode_attention call (CUDA events)."""
+    ws_bytes = pkv.decode_workspace_bytes(step.num_seqs, step.num_q_heads, step.max_seq_len,
+                                          step.block_size, part)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev["q"].device)
+    out = torch.empty_like(dev["q"])
+
+    def call():
+        pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                   dev["seq_lens"], step.num_kv_heads, step.scale, out,
+                                   max_seq_len=step.max_seq_len, partition_size=part,
+                                   workspace=ws)
+
+    eager = time_calls(call, reps, warmup)
+    if not graph:
+        return eager
+    return eager, time_calls_graph(call, flush=attention_bytes(step) < L2_FLUSH_BYTES)
+
+
 def measure_attention(pkv, step, device, label, workload):
     dev = {"q": step.q.to(device), "k_cache": step.k_cache.to(device),
            "v_cache": step.v_cache.to(device), "block_tables": step.block_tables.to(device),
            "seq_lens": step.seq_lens.to(device)}
-    ms = time_attention_only(pkv, step, dev, 0)
+    eager, ms = time_attention_only(pkv, step, dev, 0, graph=True)
     hbm, _ = measured_peaks()
     gbs = attention_bytes(step) / (ms * 1e-3) / 1e9
     del dev
     torch.cuda.empty_cache()
-    return {"workload": workload, "attention_ms": round(ms, 4), "achieved_gbs": round(gbs, 1),
+    timing = "CUDA graph replay" + (", L2 evicted before every call"
+                                    if attention_bytes(step) < L2_FLUSH_BYTES else
+                                    ", inputs larger than L2")
+    return {"workload": workload, "attention_ms": round(ms, 4), "timing": timing,
+            "host_call_ms": round(eager, 4), "achieved_gbs": round(gbs, 1),
             "frac_of_measured_peak": round(gbs / hbm, 4),
             "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "decode_tokens_per_s": round(step.num_seqs / (ms * 1e-3), 1)}
@@ -536,6 +601,26 @@ def other_workloads(pkv, W, device, all_configs):
     return extra
 
 
+def single_workload(pkv, W, device, name):
+    """One workload's decode attention (or full prefix-sharing steps) measured alone."""
+    if name == "tiny":
+        return {f"B{bs}": measure_attention(
+            pkv, W.tiny(bs), device, "tiny",
+            f"5 sequences 37/91/128/201/511, 8 heads, fp16, block {bs}") for bs in (16, 32)}
+    if name == "opt13b_like":
+        return measure_attention(
+            pkv, W.opt13b_like(), device, "opt13b_like",
+            "128 sequences, log-normal lengths (cap 2048), 40 heads MHA, fp16, block 16")
+    if name == "long_context":
+        return measure_attention(pkv, W.long_context(), device, "long_context",
+                                 "8 sequences x 32768 tokens, 32 q / 8 kv heads, bf16, block 16")
+    if name == "long_context_fp8":
+        return measure_attention_fp8(
+            pkv, W.long_context(), device,
+            "8 sequences x 32768 tokens over 8-bit pools, 32 q / 8 kv heads, bf16 queries")
+    return prefix_sharing_steps(pkv, W, device, 1040 if name == "prefix_sharing_cow" else 1024)
+
+
 def run_pkv(args, rank, world, local_rank):
     import paged_kv_cache_242_gb300 as pkv
     from paged_kv_cache_242_gb300 import workloads as W
@@ -752,6 +837,16 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.only in SINGLE_WORKLOADS:
+            import paged_kv_cache_242_gb300 as pkv
+            from paged_kv_cache_242_gb300 import workloads as W
+
+            pkv._lib.load()
+            device = torch.device("cuda", local_rank)
+            torch.cuda.set_device(device)
+            rec = single_workload(pkv, W, device, args.only)
+            if rank == 0:
+                print(json.dumps(dict(metric=METRIC, only=args.only, **rec)), flush=True)
         elif args.only == "prefill":
             import paged_kv_cache_242_gb300 as pkv
             from paged_kv_cache_242_gb300 import workloads as W

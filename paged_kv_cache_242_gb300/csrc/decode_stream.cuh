@@ -440,11 +440,13 @@ cudaError_t launch_stream(const CUtensorMap& k_map, const CUtensorMap& v_map, De
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (err != cudaSuccess) return err;
-    // enough CTAs for ~16 tiles per warp, at most one per SM
+    // enough CTAs for ~kStreamTilesPerWarp tiles per warp, at most one per SM
+    // (small batches are latency-bound: more warps, fewer tiles each)
     const int64_t max_tiles = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
                               ((a.max_seq_len + kTT - 1) / kTT);
     constexpr int kWarps = Policy<__half>::kWarps;
-    int64_t ctas = (max_tiles + kWarps * 16 - 1) / (kWarps * 16);
+    constexpr int64_t kPerCta = static_cast<int64_t>(kWarps) * kStreamTilesPerWarp;
+    int64_t ctas = (max_tiles + kPerCta - 1) / kPerCta;
     const int cap = sms < kStreamMaxCtas ? sms : kStreamMaxCtas;
     if (ctas > cap) ctas = cap;
     if (ctas < 1) ctas = 1;

@@ -98,6 +98,9 @@ struct DecodeArgs {
 #ifndef PKV_STREAM_WARPS_FP8_COLS
 #define PKV_STREAM_WARPS_FP8_COLS 8
 #endif
+#ifndef PKV_STREAM_TILES_PER_WARP
+#define PKV_STREAM_TILES_PER_WARP 4
+#endif
 #ifndef PKV_STREAM_STAGES_FP8
 #define PKV_STREAM_STAGES_FP8 2
 #endif
@@ -121,6 +124,8 @@ constexpr int kStreamMaxWarps =
     (kStreamWarps > kStreamWarpsFp8 ? kStreamWarps : kStreamWarpsFp8) > kStreamWarpsFp8Cols
         ? (kStreamWarps > kStreamWarpsFp8 ? kStreamWarps : kStreamWarpsFp8)
         : kStreamWarpsFp8Cols;
+// target tiles per warp when the grid need not fill every SM
+constexpr int kStreamTilesPerWarp = PKV_STREAM_TILES_PER_WARP;
 constexpr int kStreamMaxCtas = 160;     // cap of its grid (one CTA per SM)
 constexpr int kStreamMaxSeqs = 4096;    // sequences whose prefix fits shared memory
 constexpr int kTileTokens = 16;         // tokens per streamed tile (16-bit pools)

@@ -10,9 +10,13 @@
 // running max / running sum of Eq. (4) of "Serving Language Models Within a
 // Memory Budget".
 //
-// One CTA per (128-row tile, KV head, sequence); a row is one (query token,
-// query head of the KV head's group) pair, token-major, so the group shares
-// every key tile.  Ten warps with fixed roles:
+// Work items are (128-row tile, KV head, sequence); a row is one (query
+// token, query head of the KV head's group) pair, token-major, so the group
+// shares every key tile.  The grid is persistent (one CTA per SM): each CTA
+// walks its share of the items with one running pipeline, so tensor memory,
+// barriers and the K / V ring are set up once, and the next item's Q load
+// and first S run while the previous item's output is written.  Ten warps
+// with fixed roles:
 //   warp 0     TMA producer: K and V tiles of 64 keys (64-column boxes of the
 //              4-D pool view, 128-byte swizzle) into a six-stage ring;
 //   warp 1     tensor-core issuer (one thread): S_j = Q K_j^T with Q read
@@ -81,20 +85,52 @@ constexpr size_t kSmemBytes = 1024 + kCtlOff + sizeof(TcControl);
 // builds one descriptor per region and advances its address field by
 // (bytes >> 4).
 
+// The work list: item v = (h + H s) + H S x for row tile x (x = 0 is a
+// sequence's last, longest row tile), KV head h and sequence s.  Every role
+// of a CTA walks the same items v = blockIdx.x, + gridDim.x, ... and skips
+// the same dead ones (x past the sequence's row tiles, or invalid lengths).
+struct Item {
+    int s, h, q0, ctx, rows_total, R0, n_tiles, first_lim, n;
+};
+
+__device__ __forceinline__ bool load_item(const PrefillArgs& a, int64_t v, int X, Item& it) {
+    const int H = a.num_kv_heads;
+    const int64_t hs = v % (static_cast<int64_t>(H) * a.num_seqs);
+    const int x = static_cast<int>(v / (static_cast<int64_t>(H) * a.num_seqs));
+    (void)X;
+    it.s = static_cast<int>(hs / H);
+    it.h = static_cast<int>(hs - static_cast<int64_t>(it.s) * H);
+    it.q0 = __ldg(a.cu_q + it.s);
+    const int q_len = __ldg(a.cu_q + it.s + 1) - it.q0;
+    it.n = __ldg(a.seq_lens + it.s);
+    if (it.n < 0 || it.n > a.max_seq_len || q_len < 0 || q_len > a.max_q_len || q_len > it.n)
+        return false;
+    const int g = a.group;
+    it.ctx = it.n - q_len;
+    it.rows_total = q_len * g;
+    const int row_tiles = (it.rows_total + kRows - 1) / kRows;
+    if (x >= row_tiles) return false;
+    it.R0 = (row_tiles - 1 - x) * kRows;
+    const int last_row = min(it.R0 + kRows, it.rows_total) - 1;
+    it.n_tiles = (it.ctx + last_row / g + 1 + kKeys - 1) / kKeys;
+    it.first_lim = it.ctx + it.R0 / g;
+    return true;
+}
+
 template <typename T, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap k_map,
-                            const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
+                            const __grid_constant__ CUtensorMap v_map, const PrefillArgs a,
+                            int X) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     TcControl* ctl = reinterpret_cast<TcControl*>(sm + kCtlOff);
     const uint32_t s_base = smem_addr(sm);
-    const int h = blockIdx.y;
-    const int s = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = a.group;
+    const int64_t n_items = static_cast<int64_t>(X) * a.num_kv_heads * a.num_seqs;
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&k_map);
@@ -102,22 +138,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_wait_prerequisites();
     pdl_allow_dependents();
-
-    const int q0 = __ldg(a.cu_q + s);
-    const int q_len = __ldg(a.cu_q + s + 1) - q0;
-    const int n = __ldg(a.seq_lens + s);
-    if (n < 0 || n > a.max_seq_len || q_len < 0 || q_len > a.max_q_len || q_len > n) {
-        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) report(a.err, PKV_DEVERR_BAD_SEQ_LEN);
-        return;  // uniform over the CTA
-    }
-    const int ctx = n - q_len;
-    const int rows_total = q_len * g;
-    const int row_tiles = (rows_total + kRows - 1) / kRows;
-    if (static_cast<int>(blockIdx.x) >= row_tiles) return;
-    const int R0 = (row_tiles - 1 - static_cast<int>(blockIdx.x)) * kRows;  // longest first
-    const int last_row = min(R0 + kRows, rows_total) - 1;
-    const int n_tiles = (ctx + last_row / g + 1 + kKeys - 1) / kKeys;
-    const int first_lim = ctx + R0 / g;  // the smallest causal limit among the CTA's rows
 
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&ctl->q_full), kSoftmaxWarps);
@@ -134,6 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&ctl->stat_ready), kSoftmaxWarps);
         fence_barrier_init();
     }
+    // every sequence's lengths are checked once, spread over the grid
+    for (int s = blockIdx.x * kThreads + threadIdx.x; s < a.num_seqs; s += gridDim.x * kThreads) {
+        const int q_len = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+        const int n = __ldg(a.seq_lens + s);
+        if (n < 0 || n > a.max_seq_len || q_len < 0 || q_len > a.max_q_len || q_len > n)
+            report(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+    }
     if (warp == 1) tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
     tcgen05_before_sync();
     __syncthreads();
@@ -144,71 +171,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================ TMA producer ==============================
         constexpr int kBoxRows = BS < kKeys ? BS : kKeys;
         constexpr int kBlocksPerTile = BS < kKeys ? kKeys / BS : 1;
-        const int nblocks = (n + BS - 1) / BS;
-        const int32_t* table = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
-        int win_base = -(1 << 30), win_id = -1;
-        int issued = 0;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % kStages;
-            const int first_blk = (j * kKeys) / BS;
-            const int last_blk = min(first_blk + kBlocksPerTile - 1, nblocks - 1);
-            if (first_blk < win_base || last_blk >= win_base + 32) {
-                win_base = first_blk;
-                const int e = win_base + lane;
-                win_id = e < nblocks ? __ldg(table + e) : -1;
-            }
-            int ids[kBlocksPerTile];
-            bool ok = true;
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int b = 0; b < kBlocksPerTile; ++b) {
-                const int blk = first_blk + b;
-                ids[b] = __shfl_sync(0xffffffffu, win_id, min(max(blk - win_base, 0), 31));
-                if (blk < nblocks) {  // blocks past the sequence end are not read
-                    ok = ok && ids[b] >= 0 && ids[b] < a.num_blocks;
-                    bytes += 4 * kBoxRows * 128;  // K and V, two halves each
+        int J = 0;  // tiles issued by this CTA over all its items
+        bool alive = true;
+        for (int64_t v = blockIdx.x; alive && v < n_items; v += gridDim.x) {
+            Item it;
+            if (!load_item(a, v, X, it)) continue;
+            const int nblocks = (it.n + BS - 1) / BS;
+            const int32_t* table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
+            int win_base = -(1 << 30), win_id = -1;
+            for (int j = 0; j < it.n_tiles; ++j, ++J) {
+                const int st = J % kStages;
+                const int first_blk = (j * kKeys) / BS;
+                const int last_blk = min(first_blk + kBlocksPerTile - 1, nblocks - 1);
+                if (first_blk < win_base || last_blk >= win_base + 32) {
+                    win_base = first_blk;
+                    const int e = win_base + lane;
+                    win_id = e < nblocks ? __ldg(table + e) : -1;
                 }
-            }
-            int timed_out = 0;
-            if (lane == 0 && j >= kStages &&
-                !mbar_wait(smem_addr(&ctl->kv_empty[st]), ((j - kStages) / kStages) & 1))
-                timed_out = 1;
-            if (__shfl_sync(0xffffffffu, timed_out, 0)) {
-                if (lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
-                break;
-            }
-            if (lane == 0) {
-                const uint32_t full = smem_addr(&ctl->kv_full[st]);
-                ctl->valid[st] = ok ? 1 : 0;
-                if (ok) {
-                    const uint32_t kb = s_base + st * 2 * kTile;
-                    const uint32_t vb = kb + kTile;
-                    const int row = (j * kKeys) % BS;  // 0 unless BS > 64
-                    mbar_arrive_expect_tx(full, bytes);
+                int ids[kBlocksPerTile];
+                bool ok = true;
+                uint32_t bytes = 0;
 #pragma unroll
-                    for (int b = 0; b < kBlocksPerTile; ++b) {
-                        if (first_blk + b >= nblocks) continue;
-                        const uint32_t off = b * kBoxRows * 128;
-                        tma_load_4d(kb + off, &k_map, full, 0, row, h, ids[b]);
-                        tma_load_4d(kb + kKVHalf + off, &k_map, full, 64, row, h, ids[b]);
-                        tma_load_4d(vb + off, &v_map, full, 0, row, h, ids[b]);
-                        tma_load_4d(vb + kKVHalf + off, &v_map, full, 64, row, h, ids[b]);
+                for (int b = 0; b < kBlocksPerTile; ++b) {
+                    const int blk = first_blk + b;
+                    ids[b] = __shfl_sync(0xffffffffu, win_id, min(max(blk - win_base, 0), 31));
+                    if (blk < nblocks) {  // blocks past the sequence end are not read
+                        ok = ok && ids[b] >= 0 && ids[b] < a.num_blocks;
+                        bytes += 4 * kBoxRows * 128;  // K and V, two halves each
                     }
-                } else {
-                    report(a.err, PKV_DEVERR_BAD_BLOCK_ID);
-                    mbar_arrive(full);
                 }
+                int timed_out = 0;
+                if (lane == 0 && J >= kStages &&
+                    !mbar_wait(smem_addr(&ctl->kv_empty[st]), ((J - kStages) / kStages) & 1))
+                    timed_out = 1;
+                if (__shfl_sync(0xffffffffu, timed_out, 0)) {
+                    if (lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
+                    alive = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t full = smem_addr(&ctl->kv_full[st]);
+                    ctl->valid[st] = ok ? 1 : 0;
+                    if (ok) {
+                        const uint32_t kb = s_base + st * 2 * kTile;
+                        const uint32_t vb = kb + kTile;
+                        const int row = (j * kKeys) % BS;  // 0 unless BS > 64
+                        mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+                        for (int b = 0; b < kBlocksPerTile; ++b) {
+                            if (first_blk + b >= nblocks) continue;
+                            const uint32_t off = b * kBoxRows * 128;
+                            tma_load_4d(kb + off, &k_map, full, 0, row, it.h, ids[b]);
+                            tma_load_4d(kb + kKVHalf + off, &k_map, full, 64, row, it.h, ids[b]);
+                            tma_load_4d(vb + off, &v_map, full, 0, row, it.h, ids[b]);
+                            tma_load_4d(vb + kKVHalf + off, &v_map, full, 64, row, it.h, ids[b]);
+                        }
+                    } else {
+                        report(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+                        mbar_arrive(full);
+                    }
+                }
+                __syncwarp();
             }
-            issued = j + 1;
-            __syncwarp();
         }
         if (lane == 0) {  // leave only once this CTA's copies have landed (bounded)
-            const int first = issued > kStages ? issued - kStages : 0;
-            for (int j = first; j < issued; ++j)
+            const int first = J > kStages ? J - kStages : 0;
+            for (int j = first; j < J; ++j)
                 mbar_wait(smem_addr(&ctl->kv_full[j % kStages]), (j / kStages) & 1);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer =================================
+        // One stream of tiles J over all items: S_J is issued before
+        // P_{J-1} V_{J-1}, except at the start of an item, where the last
+        // P V of the previous item goes first (its epilogue is waiting for it).
         if (lane == 0) {
             constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
             constexpr uint32_t kIdS = umma_idesc_f16(kBf16, kRows, kKeys, false, false);
@@ -217,14 +252,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv = umma_desc_sw128(s_base + kTile, kKVHalf, 1024);
             const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
             const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
-            bool alive = mbar_wait(smem_addr(&ctl->q_full), 0);
-            for (int j = 0; alive && j <= n_tiles; ++j) {
-                if (j < n_tiles) {
-                    const int st = j % kStages, b = j & 1;
-                    alive = mbar_wait(smem_addr(&ctl->kv_full[st]), (j / kStages) & 1);
-                    // S / P buffer b is free once P_{j-2} V_{j-2} has completed
-                    if (alive && j >= 2)
-                        alive = mbar_wait(smem_addr(&ctl->o_done[b]), ((j - 2) >> 1) & 1);
+            bool alive = true;
+            int J = 0, k = 0;
+            bool pending = false;      // P_{J-1} V_{J-1} not issued yet
+            bool pending_first = false;  // ... and it is its item's first tile
+            auto issue_pv = [&](int jp, bool first_of_item) {
+                const int stp = jp % kStages, pb = jp & 1;
+                alive = mbar_wait(smem_addr(&ctl->p_full[pb]), (jp >> 1) & 1);
+                if (!alive) return;
+                tcgen05_after_sync();
+                const uint32_t vs_lo = v_lo + ((stp * 2 * kTile) >> 4);
+                const uint32_t first = first_of_item ? 0u : 1u;
+                // P of key half c lives in columns 32 c .. + 31 of the buffer:
+                // its high part in the first 16, the low part in the next 16
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int ks = 0; ks < kKeys / 16; ++ks)
+                        umma_f16_tmem_a(tmem + kOCol + 128 * (ks >> 1),
+                                        tmem + pb * kKeys + 32 * (ks >> 1) + 16 * part + 8 * (ks & 1),
+                                        vs_lo + ((ks * 16 * 128) >> 4), v_hi, kIdO,
+                                        (part > 0 || (ks & 1)) ? 1u : first);
+                }
+                umma_commit(smem_addr(&ctl->o_done[pb]));
+                umma_commit(smem_addr(&ctl->kv_empty[stp]));
+            };
+            for (int64_t v = blockIdx.x; alive && v < n_items; v += gridDim.x) {
+                Item it;
+                if (!load_item(a, v, X, it)) continue;
+                // the previous item's last P V first, then this item's Q
+                if (pending) {
+                    issue_pv(J - 1, pending_first);
+                    pending = false;
+                    if (!alive) break;
+                }
+                alive = mbar_wait(smem_addr(&ctl->q_full), k & 1);
+                if (!alive) break;
+                tcgen05_after_sync();
+                for (int j = 0; j < it.n_tiles; ++j, ++J) {
+                    const int st = J % kStages, b = J & 1;
+                    alive = mbar_wait(smem_addr(&ctl->kv_full[st]), (J / kStages) & 1);
+                    // S / P buffer b is free once P_{J-2} V_{J-2} has completed
+                    if (alive && J >= 2)
+                        alive = mbar_wait(smem_addr(&ctl->o_done[b]), ((J - 2) >> 1) & 1);
                     if (!alive) break;
                     tcgen05_after_sync();
                     const uint32_t ks_lo = k_lo + ((st * 2 * kTile) >> 4);
@@ -234,29 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         ks_lo + (((ks >> 2) * kKVHalf + (ks & 3) * 32) >> 4), k_hi,
                                         kIdS, ks > 0);
                     umma_commit(smem_addr(&ctl->s_full[b]));
-                }
-                if (j >= 1) {
-                    const int jp = j - 1, stp = jp % kStages, pb = jp & 1;
-                    alive = mbar_wait(smem_addr(&ctl->p_full[pb]), (jp >> 1) & 1);
-                    if (!alive) break;
-                    tcgen05_after_sync();
-                    const uint32_t vs_lo = v_lo + ((stp * 2 * kTile) >> 4);
-                    const uint32_t first = jp > 0 ? 1u : 0u;
-                    // P of key half c lives in columns 32 c .. + 31 of the buffer:
-                    // its high part in the first 16, the low part in the next 16
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                        for (int ks = 0; ks < kKeys / 16; ++ks)
-                            umma_f16_tmem_a(tmem + kOCol + 128 * (ks >> 1),
-                                            tmem + pb * kKeys + 32 * (ks >> 1) + 16 * part + 8 * (ks & 1),
-                                            vs_lo + ((ks * 16 * 128) >> 4), v_hi, kIdO,
-                                            (part > 0 || (ks & 1)) ? 1u : first);
+                    if (pending) {  // P V of this item's previous tile
+                        issue_pv(J - 1, pending_first);
+                        if (!alive) break;
                     }
-                    umma_commit(smem_addr(&ctl->o_done[pb]));
-                    umma_commit(smem_addr(&ctl->kv_empty[stp]));
+                    pending = true;
+                    pending_first = j == 0;
                 }
+                ++k;
             }
+            if (alive && pending) issue_pv(J - 1, pending_first);
             if (!alive) report(a.err, PKV_DEVERR_TIMEOUT);
             umma_commit(smem_addr(&ctl->mma_done));  // every MMA above has completed
             mbar_wait(smem_addr(&ctl->mma_done), 0);
@@ -270,148 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes 32 quarter .. + 31 are this warp's
         const int half = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
-        const int R = R0 + r;
-        const bool live = R < rows_total;
-        const int t = R / g;
-        const int lim = live ? ctx + t : -1;  // last key this row sees
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const size_t out_row =
-            (static_cast<size_t>(q0 + t) * a.num_q_heads + static_cast<size_t>(h) * g + R % g) *
-            kHeadDim;
         const float sl = a.scale_log2;
-        // ---- dims 64 half .. + 63 of Q row r into TMEM (zeros past the last row) ----
-        {
-            const uint4* src =
-                reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + out_row) + 8 * half;
-            uint32_t w[32];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                w[4 * c] = v.x;
-                w[4 * c + 1] = v.y;
-                w[4 * c + 2] = v.z;
-                w[4 * c + 3] = v.w;
-            }
-            tmem_st32(tmem + lane_base + kQCol + 32 * half, w);
-            tmem_st_wait();
-            tcgen05_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->q_full));
-        }
-        float m_used = -INFINITY, l = 0.f;
         bool alive = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1, st = j % kStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->s_full[b]), (j >> 1) & 1))) {
-                alive = false;
-                break;
-            }
-            tcgen05_after_sync();
-            const int key0 = j * kKeys + 32 * half;
-            const bool masked = j * kKeys + kKeys - 1 > first_lim;
-            const uint32_t sp_addr = tmem + lane_base + b * kKeys + 32 * half;
-            uint32_t v[32];
-            tmem_ld32(sp_addr, v);
-            tmem_ld_wait();
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float x = __uint_as_float(v[i]) * sl;
-                if (masked) x = key0 + i <= lim ? x : -INFINITY;  // also drops NaN
-                mx[i & 3] = fmaxf(mx[i & 3], x);
-            }
-            const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            // lazy rescale: keep the older max until this half's max exceeds it by 2^8
-            const float m_new = fmaxf(m_used, row_max);
-            const bool bump = m_new > m_used + kRescaleLog2;  // true at the first finite max
-            const float m_tgt = bump ? m_new : m_used;
-            const float base = m_tgt == -INFINITY ? 0.f : m_tgt;
-            const float alpha = bump ? ex2(m_used - base) : 1.f;  // 0 while m_used = -inf
-            m_used = m_tgt;
-
-            if (j >= 1 && __any_sync(0xffffffffu, bump)) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->o_done[(j - 1) & 1]),
-                                                       ((j - 1) >> 1) & 1))) {
-                    alive = false;
-                    break;
-                }
-                tcgen05_after_sync();
-#pragma unroll 1
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t ov[32];
-                    const uint32_t o_addr = tmem + lane_base + kOCol + 128 * half + 32 * c4;
-                    tmem_ld32(o_addr, ov);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(o_addr, ov);
-                }
-                tmem_st_wait();
-            }
-            // V rows of keys past the sequence end hold stale bytes: zero them
-            if (j * kKeys + kKeys > n) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(smem_addr(&ctl->kv_full[st]), (j / kStages) & 1))) {
-                    alive = false;
-                    break;
-                }
-                if (r < kKeys && j * kKeys + r >= n) {
-                    const uint32_t vrow = s_base + st * 2 * kTile + kTile + half * kKVHalf + r * 128;
-                    asm volatile(
-                        "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
-                        "st.shared.v4.b32 [%0], {z, z, z, z};\n\tst.shared.v4.b32 [%0+16], {z, z, z, z};\n\t"
-                        "st.shared.v4.b32 [%0+32], {z, z, z, z};\n\tst.shared.v4.b32 [%0+48], {z, z, z, z};\n\t"
-                        "st.shared.v4.b32 [%0+64], {z, z, z, z};\n\tst.shared.v4.b32 [%0+80], {z, z, z, z};\n\t"
-                        "st.shared.v4.b32 [%0+96], {z, z, z, z};\n\tst.shared.v4.b32 [%0+112], {z, z, z, z};\n\t}"
-                        ::"r"(vrow) : "memory");
-                }
-                fence_proxy_async_shared();
-            }
-            // ---- weights, their sum, P's high / low parts over these 32 columns ----
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float x = fmaf(__uint_as_float(v[i]), sl, -base);
-                if (masked) x = key0 + i <= lim ? x : -INFINITY;
-                const float p = ex2(x);
-                ps[i & 3] += p;
-                v[i] = __float_as_uint(p);
-            }
-            uint32_t pw[32];  // high parts of keys 0-31 of this half, then the low parts
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float p0 = __uint_as_float(v[2 * e]), p1 = __uint_as_float(v[2 * e + 1]);
-                pw[e] = Mma<T>::pack(p0, p1);
-                const float2 back = Mma<T>::unpack(pw[e]);
-                pw[16 + e] = Mma<T>::pack(p0 - back.x, p1 - back.y);
-            }
-            tmem_st32(sp_addr, pw);
-            tmem_st_wait();
-            l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-            tcgen05_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->p_full[b]));
-        }
-        // ---- epilogue: merge the two key halves (Eq. 4), O / l to the output ------
-        if (alive) {
+        int J = 0, ep = 0;
+        // the previous item's epilogue runs after the next item's Q is in place
+        bool prev = false;
+        bool prev_live = false;
+        size_t prev_out = 0;
+        float prev_m = -INFINITY, prev_l = 0.f;
+        int prev_last = 0;  // global index of the previous item's last tile
+        auto epilogue = [&]() {
+            // ---- merge the two key halves (Eq. 4), O / l to the output ------
             const uint32_t st_addr = tmem + lane_base + kStatCol;
-            tmem_st1(st_addr + 2 * half, __float_as_uint(m_used));
-            tmem_st1(st_addr + 2 * half + 1, __float_as_uint(l));
+            alive = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->o_done[prev_last & 1]),
+                                                      (prev_last >> 1) & 1));
+            if (!alive) return;
+            tcgen05_after_sync();
+            tmem_st1(st_addr + 2 * half, __float_as_uint(prev_m));
+            tmem_st1(st_addr + 2 * half + 1, __float_as_uint(prev_l));
             tmem_st_wait();
             tcgen05_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&ctl->stat_ready));
-            alive = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->stat_ready), 0)) &&
-                    __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->o_done[(n_tiles - 1) & 1]),
-                                                      ((n_tiles - 1) >> 1) & 1));
-        }
-        if (!alive) {
-            if (lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
-        } else {
+            alive = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->stat_ready), ep & 1));
+            ++ep;
+            if (!alive) return;
             tcgen05_after_sync();
-            const uint32_t st_addr = tmem + lane_base + kStatCol;
             const float m0 = __uint_as_float(tmem_ld1(st_addr));
             const float l0 = __uint_as_float(tmem_ld1(st_addr + 1));
             const float m1 = __uint_as_float(tmem_ld1(st_addr + 2));
@@ -423,14 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float den = l0 * w0 + l1 * w1;
             const float inv = den > 0.f ? 1.f / den : 0.f;
             const float f0 = w0 * inv, f1 = w1 * inv;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + out_row) + 8 * half;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + prev_out) + 8 * half;
 #pragma unroll 1
             for (int c2 = 0; c2 < 2; ++c2) {  // output dims 64 half + 32 c2 ..
                 uint32_t oa[32], ob[32];
                 tmem_ld32(tmem + lane_base + kOCol + 64 * half + 32 * c2, oa);
                 tmem_ld32(tmem + lane_base + kOCol + 128 + 64 * half + 32 * c2, ob);
                 tmem_ld_wait();
-                if (live) {
+                if (prev_live) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t w[4];
@@ -445,7 +387,149 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // O is read: the next item's first P V may overwrite it
+            tcgen05_before_sync();
+        };
+        for (int64_t v = blockIdx.x; alive && v < n_items; v += gridDim.x) {
+            Item it;
+            if (!load_item(a, v, X, it)) continue;
+            const int R = it.R0 + r;
+            const bool live = R < it.rows_total;
+            const int t = R / g;
+            const int lim = live ? it.ctx + t : -1;  // last key this row sees
+            const size_t out_row = (static_cast<size_t>(it.q0 + t) * a.num_q_heads +
+                                    static_cast<size_t>(it.h) * g + R % g) *
+                                   kHeadDim;
+            // ---- dims 64 half .. + 63 of Q row r into TMEM (zeros past the last
+            // row); every S of the previous item has completed (its last s_full
+            // was waited for), so its Q may be overwritten
+            {
+                const uint4* src =
+                    reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + out_row) + 8 * half;
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 q4 = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * c] = q4.x;
+                    w[4 * c + 1] = q4.y;
+                    w[4 * c + 2] = q4.z;
+                    w[4 * c + 3] = q4.w;
+                }
+                tmem_st32(tmem + lane_base + kQCol + 32 * half, w);
+                tmem_st_wait();
+                tcgen05_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->q_full));
+            }
+            if (prev) {
+                epilogue();
+                if (!alive) break;
+            }
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.n_tiles; ++j, ++J) {
+                const int b = J & 1, st = J % kStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->s_full[b]), (J >> 1) & 1))) {
+                    alive = false;
+                    break;
+                }
+                tcgen05_after_sync();
+                const int key0 = j * kKeys + 32 * half;
+                const bool masked = j * kKeys + kKeys - 1 > it.first_lim;
+                const uint32_t sp_addr = tmem + lane_base + b * kKeys + 32 * half;
+                uint32_t v[32];
+                tmem_ld32(sp_addr, v);
+                tmem_ld_wait();
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(v[i]) * sl;
+                    if (masked) x = key0 + i <= lim ? x : -INFINITY;  // also drops NaN
+                    mx[i & 3] = fmaxf(mx[i & 3], x);
+                }
+                const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // lazy rescale: keep the older max until this half's max exceeds it by 2^8
+                const float m_new = fmaxf(m_used, row_max);
+                const bool bump = m_new > m_used + kRescaleLog2;  // true at the first finite max
+                const float m_tgt = bump ? m_new : m_used;
+                const float base = m_tgt == -INFINITY ? 0.f : m_tgt;
+                const float alpha = bump ? ex2(m_used - base) : 1.f;  // 0 while m_used = -inf
+                m_used = m_tgt;
+
+                if (j >= 1 && __any_sync(0xffffffffu, bump)) {
+                    // O must hold P_{J-1} V_{J-1} before it is rescaled
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->o_done[(J - 1) & 1]),
+                                                           ((J - 1) >> 1) & 1))) {
+                        alive = false;
+                        break;
+                    }
+                    tcgen05_after_sync();
+#pragma unroll 1
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t ov[32];
+                        const uint32_t o_addr = tmem + lane_base + kOCol + 128 * half + 32 * c4;
+                        tmem_ld32(o_addr, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(o_addr, ov);
+                    }
+                    tmem_st_wait();
+                }
+                // V rows of keys past the sequence end hold stale bytes: zero them
+                if (j * kKeys + kKeys > it.n) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(smem_addr(&ctl->kv_full[st]), (J / kStages) & 1))) {
+                        alive = false;
+                        break;
+                    }
+                    if (r < kKeys && j * kKeys + r >= it.n) {
+                        const uint32_t vrow =
+                            s_base + st * 2 * kTile + kTile + half * kKVHalf + r * 128;
+                        asm volatile(
+                            "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
+                            "st.shared.v4.b32 [%0], {z, z, z, z};\n\tst.shared.v4.b32 [%0+16], {z, z, z, z};\n\t"
+                            "st.shared.v4.b32 [%0+32], {z, z, z, z};\n\tst.shared.v4.b32 [%0+48], {z, z, z, z};\n\t"
+                            "st.shared.v4.b32 [%0+64], {z, z, z, z};\n\tst.shared.v4.b32 [%0+80], {z, z, z, z};\n\t"
+                            "st.shared.v4.b32 [%0+96], {z, z, z, z};\n\tst.shared.v4.b32 [%0+112], {z, z, z, z};\n\t}"
+                            ::"r"(vrow) : "memory");
+                    }
+                    fence_proxy_async_shared();
+                }
+                // ---- weights, their sum, P's high / low parts over these 32 columns ----
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = fmaf(__uint_as_float(v[i]), sl, -base);
+                    if (masked) x = key0 + i <= lim ? x : -INFINITY;
+                    const float p = ex2(x);
+                    ps[i & 3] += p;
+                    v[i] = __float_as_uint(p);
+                }
+                uint32_t pw[32];  // high parts of keys 0-31 of this half, then the low parts
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = __uint_as_float(v[2 * e]), p1 = __uint_as_float(v[2 * e + 1]);
+                    pw[e] = Mma<T>::pack(p0, p1);
+                    const float2 back = Mma<T>::unpack(pw[e]);
+                    pw[16 + e] = Mma<T>::pack(p0 - back.x, p1 - back.y);
+                }
+                tmem_st32(sp_addr, pw);
+                tmem_st_wait();
+                l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+                tcgen05_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->p_full[b]));
+            }
+            prev = true;
+            prev_live = live;
+            prev_out = out_row;
+            prev_m = m_used;
+            prev_l = l;
+            prev_last = J - 1;
         }
+        if (alive && prev) epilogue();
+        if (!alive && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     }
 
     // every role is done with TMEM (the issuer waited for its last MMA)
@@ -463,10 +547,17 @@ cudaError_t launch_tc_typed(const CUtensorMap& k_map, const CUtensorMap& v_map,
     cudaError_t err = ensure_smem_limit<paged_prefill_tc_kernel<T, BS>>(kSmemBytes);
     if (err != cudaSuccess) return err;
     const int64_t row_tiles = (static_cast<int64_t>(a.max_q_len) * a.group + kRows - 1) / kRows;
-    dim3 grid(static_cast<unsigned>(row_tiles > 0 ? row_tiles : 1),
-              static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(a.num_seqs));
-    return launch_pdl(paged_prefill_tc_kernel<T, BS>, grid, dim3(kThreads), kSmemBytes, stream,
-                      k_map, v_map, a);
+    const int X = static_cast<int>(row_tiles > 0 ? row_tiles : 1);
+    const int64_t items = static_cast<int64_t>(X) * a.num_kv_heads * a.num_seqs;
+    int device = 0, sms = 0;
+    err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (err != cudaSuccess) return err;
+    // persistent: one CTA per SM walks the work list
+    const int ctas = static_cast<int>(items < sms ? items : sms);
+    return launch_pdl(paged_prefill_tc_kernel<T, BS>, dim3(ctas > 0 ? ctas : 1), dim3(kThreads),
+                      kSmemBytes, stream, k_map, v_map, a, X);
 }
 
 template <typename T>

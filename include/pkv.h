@@ -193,14 +193,15 @@ PKV_API pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache
  * Products of fp16/bf16 inputs accumulate in fp32; the output is rounded to
  * the storage dtype.
  *
- *   q             [total query tokens][num_q_heads][head_dim], contiguous;
- *                 sequence s's queries are rows cu_seqlens_q[s] ..
- *                 cu_seqlens_q[s+1] - 1.
+ *   q             [total query tokens][num_q_heads][head_dim], contiguous,
+ *                 16-byte aligned (rows move as 16-byte vectors); sequence
+ *                 s's queries are rows cu_seqlens_q[s] .. cu_seqlens_q[s+1] - 1.
  *   cu_seqlens_q  DEVICE [num_seqs + 1] int32, non-decreasing, from 0.
  *   max_q_len     HOST value >= every q_len_s (sizes the launch).
  *   k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
  *   max_seq_len, scale: as pkv_paged_decode_attention.
- *   out           [total query tokens][num_q_heads][head_dim].
+ *   out           [total query tokens][num_q_heads][head_dim], 16-byte aligned.
+ * A q or out that is not 16-byte aligned returns PKV_ERR_INVALID_ARG.
  * A sequence whose q_len is negative, above max_q_len or above its
  * seq_len, or whose seq_len exceeds max_seq_len, is skipped and sets
  * PKV_DEVERR_BAD_SEQ_LEN.  Supported: head_dim 128, block_size 8, 16, 32,

@@ -280,7 +280,8 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
     if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
     if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
         return PKV_ERR_INVALID_ARG;
-    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+    // q and out rows move as 16-byte vectors
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(cu_seqlens_q, 4))
         return PKV_ERR_INVALID_ARG;
     const int64_t row_tiles =

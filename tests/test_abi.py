@@ -140,6 +140,9 @@ def test_host_validation_without_launch(lib):
     assert prefill(desc=_desc(head_dim=64)) == 2
     assert prefill(desc=_desc(block_size=24), msl=48) == 2
     assert prefill(S=0) == 0 and prefill(mq=0) == 0
+    # q and out rows move as 16-byte vectors: 4-byte aligned is refused
+    assert prefill(q=ctypes.c_void_p(0x10004)) == 1
+    assert prefill(out=ctypes.c_void_p(0x10008)) == 1
     # copy_blocks
     assert lib.pkv_copy_blocks(fake, fake, _desc(), null, 3, null, null) == 1
     assert lib.pkv_copy_blocks(null, null, _desc(), null, 0, null, null) == 0

@@ -68,6 +68,29 @@ constexpr uint32_t kTmemPerTile = 256;      // S / P buffers + 0, + 64; O + 128
 constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.f;
 
+// Packed two-lane fp32 arithmetic (one sm_100+ .f32x2 instruction for a
+// pair; each lane rounds exactly as the scalar instruction does).
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b));
+}
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
+        "mov.b64 rc, {%5, %5};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 struct alignas(8) TcControl {
     uint64_t q_full[2];     // [Q tile]: its rows are in shared memory (4 warps)
     uint64_t kv_full[kStages];
@@ -477,10 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    float x = __uint_as_float(v[i]) * sl;
-                    if (masked) x = key0 + i <= lim ? x : -INFINITY;  // also drops NaN
-                    mx[i & 3] = fmaxf(mx[i & 3], x);
+                for (int i = 0; i < 64; i += 2) {
+                    float x0, x1;
+                    mul2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl);
+                    if (masked) {
+                        x0 = key0 + i <= lim ? x0 : -INFINITY;  // also drops NaN
+                        x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
+                    }
+                    mx[i & 3] = fmaxf(mx[i & 3], x0);
+                    mx[(i + 1) & 3] = fmaxf(mx[(i + 1) & 3], x1);
                 }
                 const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 // lazy rescale: keep the older max until the row max exceeds it by 2^8
@@ -516,12 +544,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- weights, their sum, P's high / low parts over these columns ----
                 float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    float x = fmaf(__uint_as_float(v[i]), sl, -base);
-                    if (masked) x = key0 + i <= lim ? x : -INFINITY;
-                    const float p = ex2(x);
-                    ps[i & 3] += p;
-                    v[i] = __float_as_uint(p);
+                for (int i = 0; i < 64; i += 2) {
+                    float x0, x1;
+                    fma2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl, -base);
+                    if (masked) {
+                        x0 = key0 + i <= lim ? x0 : -INFINITY;
+                        x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
+                    }
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    const int a2 = (i >> 1) & 1;
+                    add2(ps[2 * a2], ps[2 * a2 + 1], ps[2 * a2], ps[2 * a2 + 1], p0, p1);
+                    v[i] = __float_as_uint(p0);
+                    v[i + 1] = __float_as_uint(p1);
                 }
                 uint32_t pw[32];
 #pragma unroll
@@ -531,8 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {  // the low part of the remainder beside it
                     const float2 back = Mma<T>::unpack(pw[e]);
-                    pw[e] = Mma<T>::pack(__uint_as_float(v[2 * e]) - back.x,
-                                         __uint_as_float(v[2 * e + 1]) - back.y);
+                    float r0, r1;
+                    sub2(r0, r1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), back.x,
+                         back.y);
+                    pw[e] = Mma<T>::pack(r0, r1);
                 }
                 tmem_st32(sp_addr + 32, pw);
                 tmem_st_wait();

@@ -41,7 +41,7 @@ def _reference(step):
                           step.seq_lens.numpy(), step.scale, step.dtype, num_threads=THREADS)
 
 
-@pytest.mark.parametrize("B", [8, 16, 32, 128])
+@pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("heads", [(8, 8), (32, 8), (16, 2), (24, 8), (20, 4)])
 def test_prefill_ragged(B, heads):
     """Contexts and prompt lengths around 16-token sub-tiles and 64- / 128-key tiles; groups of
@@ -56,6 +56,26 @@ def test_prefill_ragged(B, heads):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_attention_close(out, ref, f"prefill B={B} heads={heads}")
+
+
+def test_prefill_many_items_per_cta():
+    """More (256-row item, KV head, sequence) work items than CTAs: the grid is persistent, so
+    each CTA carries its pipeline across many items.  The second Q tile of a sequence's last
+    item is empty, partly filled or full; some sequences have no queries or nothing at all."""
+    g = torch.Generator().manual_seed(12)
+    S = 180
+    ctx = torch.randint(0, 120, (S,), generator=g).tolist()
+    ql = torch.randint(0, 81, (S,), generator=g).tolist()
+    ctx[3], ql[3] = 0, 0  # an empty sequence
+    ql[4] = 0  # cached context, no queries
+    ql[5], ql[6], ql[7], ql[8] = 32, 33, 64, 65  # 128 / 132 / 256 / 260 rows at 4 heads a group
+    step = W.build_prefill_step("many", ctx, ql, 32, 8, 16, "bfloat16", seed=12)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(step, err)
+    ref = _reference(step)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, "prefill many items")
 
 
 def test_prefill_fp16_and_mqa():

@@ -46,7 +46,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 SINGLE_WORKLOADS = ("tiny", "opt13b_like", "long_context", "long_context_fp8", "prefix_sharing",
-                    "prefix_sharing_cow")
+                    "prefix_sharing_cow", "swap")
 
 
 def parse_args():
@@ -509,10 +509,28 @@ def swap_throughput(pkv, W, device, victims=16, reps=20):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
         res[name] = {"ms": round(ms, 4), "gbs": round(n * block_bytes / (ms * 1e-3) / 1e9, 1)}
-    del k_dev, v_dev
+    # the link's bound: one contiguous copy engine transfer of the same bytes each way
+    flat_host = torch.empty(n * block_bytes, dtype=torch.uint8).pin_memory()
+    flat_dev = torch.empty(n * block_bytes, dtype=torch.uint8, device=device)
+    for name, (dst, src) in (("out_d2h", (flat_host, flat_dev)), ("in_h2d", (flat_dev, flat_host))):
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = n * block_bytes / (ms * 1e-3) / 1e9
+        res[name]["contiguous_copy_gbs"] = round(gbs, 1)
+        res[name]["frac_of_contiguous_copy"] = round(res[name]["gbs"] / gbs, 4)
+    del k_dev, v_dev, flat_dev
     torch.cuda.empty_cache()
     return {"workload": f"all {n} blocks ({n * block_bytes / 1e6:.1f} MB of K+V) of {victims} "
                         "GQA-batch sequences, device <-> page-locked host pool, one launch",
+            "bound": "the CPU-GPU link: one contiguous copy of the same bytes (copy engine)",
             **res}
 
 
@@ -618,6 +636,8 @@ def single_workload(pkv, W, device, name):
         return measure_attention_fp8(
             pkv, W.long_context(), device,
             "8 sequences x 32768 tokens over 8-bit pools, 32 q / 8 kv heads, bf16 queries")
+    if name == "swap":
+        return swap_throughput(pkv, W, device)
     return prefix_sharing_steps(pkv, W, device, 1040 if name == "prefix_sharing_cow" else 1024)
 
 

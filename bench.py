@@ -46,7 +46,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 SINGLE_WORKLOADS = ("tiny", "opt13b_like", "long_context", "long_context_fp8", "prefix_sharing",
-                    "prefix_sharing_cow", "swap")
+                    "prefix_sharing_cow", "swap", "writes")
 
 
 def parse_args():
@@ -614,9 +614,46 @@ def other_workloads(pkv, W, device, all_configs):
             sweep[str(bs)] = rec
         extra["block_size_sweep_gqa_batch"] = sweep
         extra["swap_gqa_batch"] = swap_throughput(pkv, W, device)
+        extra["writes_and_copies"] = writes_throughput(pkv, W, device)
         extra["prefix_sharing"] = prefix_sharing_steps(pkv, W, device, 1024)
         extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
     return extra
+
+
+def writes_throughput(pkv, W, device, n_pairs=2000):
+    """kv_write (one decode token per sequence, and a whole prefill batch) and
+    copy_blocks (scattered block pairs), each as a CUDA-graph replay."""
+    hbm, _ = measured_peaks()
+    res = {}
+    st = W.gqa_batch()
+    kc, vc = st.k_cache.to(device), st.v_cache.to(device)
+    pre = W.prefill_batch()
+    pk, pv, ps = pre.k_new.to(device), pre.v_new.to(device), pre.slot_mapping.to(device)
+    pkc, pvc = pre.k_cache.to(device), pre.v_cache.to(device)
+    dk, dv, dsm = st.k_new.to(device), st.v_new.to(device), st.slot_mapping.to(device)
+    # distinct sources and destinations drawn from the pool (a seeded permutation)
+    g = torch.Generator().manual_seed(11)
+    perm = torch.randperm(kc.shape[0], generator=g)[: 2 * n_pairs]
+    pairs = torch.stack([perm[:n_pairs], perm[n_pairs:]], 1).to(torch.int64).to(device)
+    block_bytes = st.num_kv_heads * st.block_size * st.head_dim * 2 * 2  # K and V
+    cases = {
+        "kv_write_decode": (lambda: pkv.kv_write(dk, dv, dsm, kc, vc),
+                            kv_write_bytes(st), f"{st.num_seqs} tokens, 8 kv heads, bf16"),
+        "kv_write_prefill": (lambda: pkv.kv_write(pk, pv, ps, pkc, pvc), kv_write_bytes(pre),
+                             f"{int(ps.numel())} prompt tokens, 8 kv heads, bf16"),
+        "copy_blocks": (lambda: pkv.copy_blocks(kc, vc, pairs), n_pairs * block_bytes * 2 + 16 * n_pairs,
+                        f"{n_pairs} scattered pairs of 16-token blocks, 8 kv heads, bf16 "
+                        "(K and V read and written)"),
+    }
+    for name, (call, nbytes, what) in cases.items():
+        ms = time_calls_graph(call, flush=nbytes < L2_FLUSH_BYTES)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"workload": what, "us": round(ms * 1e3, 2), "bytes": int(nbytes),
+                     "gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / hbm, 4),
+                     "timing": "CUDA graph replay, L2 evicted before every call"}
+    del kc, vc, pkc, pvc
+    torch.cuda.empty_cache()
+    return res
 
 
 def single_workload(pkv, W, device, name):
@@ -638,6 +675,8 @@ def single_workload(pkv, W, device, name):
             "8 sequences x 32768 tokens over 8-bit pools, 32 q / 8 kv heads, bf16 queries")
     if name == "swap":
         return swap_throughput(pkv, W, device)
+    if name == "writes":
+        return writes_throughput(pkv, W, device)
     return prefix_sharing_steps(pkv, W, device, 1040 if name == "prefix_sharing_cow" else 1024)
 
 

@@ -24,9 +24,10 @@
 //   warps 1-2  tensor-core issuers (one thread each), warp 1 for Q tile A and
 //              warp 2 for B: for each key tile S = Q K^T (Q and K from shared
 //              memory), then O += P V of the previous key tile (P read from
-//              tensor memory, V from shared memory), P split into a bf16 /
-//              fp16 high part and the low part of the remainder (two MMAs per
-//              step, so the weights keep about 16 significant bits).  With an
+//              tensor memory, V from shared memory).  With bf16 inputs P is
+//              split into a bf16 high part and the low part of the remainder
+//              (two MMAs per step, so the weights keep about 16 significant
+//              bits); with fp16 inputs P is one binary16 value (11 bits).  With an
 //              issuer per tile neither tile's S waits behind the other's
 //              softmax;
 //   warps 3-6  softmax of Q tile A, warps 7-10 of Q tile B, one thread per row
@@ -67,6 +68,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemPerTile = 256;      // S / P buffers + 0, + 64; O + 128
 constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.f;
+
+// P's 16-bit parts: bf16 keeps 8 significant bits, so P is split into a high
+// part and the low part of the remainder; binary16 keeps 11 and goes whole.
+template <typename T>
+constexpr int kPParts = std::is_same<T, __nv_bfloat16>::value ? 2 : 1;
 
 // Packed two-lane fp32 arithmetic (one sm_100+ .f32x2 instruction for a
 // pair; each lane rounds exactly as the scalar instruction does).
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t vs_lo = v_lo + ((stp * 2 * kTile) >> 4);
                 const uint32_t first = pend_first ? 0u : 1u;
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
+                for (int part = 0; part < kPParts<T>; ++part) {
 #pragma unroll
                     for (int ks = 0; ks < kKeys / 16; ++ks)
                         umma_f16_tmem_a(tq + kOCol, tq + 64 * pb + 32 * part + 8 * ks,
@@ -562,15 +568,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; ++e)
                     pw[e] = Mma<T>::pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
                 tmem_st32(sp_addr, pw);
+                if constexpr (kPParts<T> == 2) {  // the low part of the remainder beside it
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {  // the low part of the remainder beside it
-                    const float2 back = Mma<T>::unpack(pw[e]);
-                    float r0, r1;
-                    sub2(r0, r1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), back.x,
-                         back.y);
-                    pw[e] = Mma<T>::pack(r0, r1);
+                    for (int e = 0; e < 32; ++e) {
+                        const float2 back = Mma<T>::unpack(pw[e]);
+                        float r0, r1;
+                        sub2(r0, r1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]),
+                             back.x, back.y);
+                        pw[e] = Mma<T>::pack(r0, r1);
+                    }
+                    tmem_st32(sp_addr + 32, pw);
                 }
-                tmem_st32(sp_addr + 32, pw);
                 tmem_st_wait();
                 l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
                 tcgen05_before_sync();

@@ -78,6 +78,19 @@ def test_prefill_many_items_per_cta():
     assert_attention_close(out, ref, "prefill many items")
 
 
+@pytest.mark.parametrize("B", [16, 128])
+def test_prefill_fp16_ragged(B):
+    """fp16 inputs: the tensor-core kernel keeps P as one binary16 value (no low part)."""
+    step = W.build_prefill_step("ragged16", [0, 5, 16, 100, 0, 37, 600], [1, 7, 16, 65, 200, 64, 700],
+                                32, 8, B, "float16", seed=200 + B)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(step, err)
+    ref = _reference(step)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, f"prefill fp16 B={B}")
+
+
 def test_prefill_fp16_and_mqa():
     step = W.build_prefill_step("fp16", [300, 0], [129, 255], 8, 1, 16, "float16", seed=7)
     out, _ = _run(step)

@@ -194,8 +194,9 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # CPU oracle timing (baseline and reference arm)
 # ----------------------------------------------------------------------------
-def oracle_sample_rate(step, max_seconds: float, max_seqs=None, min_reps=1):
-    """Run the oracle (kv_write replay + attention) on the first sequences.
+def oracle_sample_rate(step, max_seconds: float, max_seqs=None, min_reps=1, threads=None):
+    """Run the oracle (kv_write replay + attention) on the first sequences,
+    with `threads` OpenMP threads (default: every host core).
 
     Returns (bytes per second, seconds, description, threads).
     """
@@ -205,7 +206,7 @@ def oracle_sample_rate(step, max_seconds: float, max_seqs=None, min_reps=1):
     from paged_kv_cache_242_gb300.workloads import bits
 
     S = step.num_seqs if max_seqs is None else min(max_seqs, step.num_seqs)
-    threads = oracle.max_threads()
+    threads = oracle.max_threads() if threads is None else int(threads)
     kc, vc = bits(step.k_cache), bits(step.v_cache)
     q = np.ascontiguousarray(bits(step.q)[:S])
     bt = np.ascontiguousarray(step.block_tables.numpy()[:S])
@@ -927,6 +928,10 @@ def run_pkv(args, rank, world, local_rank):
         rate, _, desc, threads = oracle_sample_rate(step, 10.0)
         cpu = {"kind": "oracle", "value": round(rate / 1e9, 4), "unit": UNIT, "cores": threads,
                "sample": desc}
+        # the same oracle on one core, on the first 8 sequences
+        rate1, _, desc1, _ = oracle_sample_rate(step, 5.0, max_seqs=8, threads=1)
+        cpu["single_core"] = {"value": round(rate1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                              "sample": desc1}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),

@@ -46,7 +46,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 SINGLE_WORKLOADS = ("tiny", "opt13b_like", "long_context", "long_context_fp8", "prefix_sharing",
-                    "prefix_sharing_cow", "swap", "writes")
+                    "prefix_sharing_cow", "swap", "writes", "beam_search")
 
 
 def parse_args():
@@ -427,10 +427,10 @@ def measure_attention_fp8(pkv, step, device, workload, reps=200, warmup=10):
             "decode_tokens_per_s": round(step.num_seqs / (ms * 1e-3), 1)}
 
 
-def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
-    """Full decode steps (copy-on-write copies + kv_write + attention) of the
-    prefix-sharing scenario, all 256 steps' inputs resident on the device."""
-    sc = W.PrefixSharingScenario(prompt_len=prompt_len, decode_steps=steps)
+def scenario_steps(pkv, device, sc, steps, physical_blocks):
+    """Full decode steps of a block-sharing scenario (copy-on-write copies +
+    kv_write + attention), every step's inputs resident on the device, the
+    pools restored between an untimed and the timed pass."""
     k_cache, v_cache = sc.k_cache.to(device), sc.v_cache.to(device)
     plan = []
     logical = unique = copies = 0
@@ -440,12 +440,16 @@ def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
                      ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens", "cow_pairs")}
                     | {"max_seq_len": st.max_seq_len, "step": st})
         logical += attention_bytes(st)
-        unique += sc.unique_blocks_in_use() * sc.num_kv_heads * sc.block_size * sc.head_dim * 4
+        unique += physical_blocks() * sc.num_kv_heads * sc.block_size * sc.head_dim * 4
         copies += int(st.cow_pairs.shape[0])
-    ws_bytes = max(pkv.decode_workspace_bytes(sc.num_seqs, sc.num_q_heads, p["max_seq_len"],
-                                              sc.block_size) for p in plan)
+    ws_bytes = max(pkv.decode_workspace_bytes(int(p["q"].shape[0]), sc.num_q_heads,
+                                              p["max_seq_len"], sc.block_size) for p in plan)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
-    out = torch.empty_like(plan[0]["q"])
+    outs = {int(p["q"].shape[0]): None for p in plan}
+    for S in outs:
+        outs[S] = torch.empty((S, sc.num_q_heads, sc.head_dim), dtype=plan[0]["q"].dtype,
+                              device=device)
+    tokens = sum(int(p["q"].shape[0]) for p in plan)
 
     def run_all():
         for p in plan:
@@ -453,7 +457,8 @@ def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
                 pkv.copy_blocks(k_cache, v_cache, p["cow_pairs"])
             pkv.kv_write(p["k_new"], p["v_new"], p["slot_mapping"], k_cache, v_cache)
             pkv.paged_decode_attention(p["q"], k_cache, v_cache, p["block_tables"], p["seq_lens"],
-                                       sc.num_kv_heads, p["step"].scale, out,
+                                       sc.num_kv_heads, p["step"].scale,
+                                       outs[int(p["q"].shape[0])],
                                        max_seq_len=p["max_seq_len"], workspace=ws)
 
     run_all()  # warm-up pass (also replays the copies and writes once)
@@ -469,16 +474,34 @@ def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     hbm, _ = measured_peaks()
-    return {"workload": f"16 prompts x {prompt_len} tokens x 8 samples, {steps} decode steps, "
-                        "block 32, 32 q / 8 kv heads, bf16",
-            "ms_per_step": round(ms / steps, 4),
-            "decode_tokens_per_s": round(sc.num_seqs * steps / (ms * 1e-3), 1),
+    return {"ms_per_step": round(ms / steps, 4),
+            "decode_tokens_per_s": round(tokens / (ms * 1e-3), 1),
             "cow_copies": copies,
             "logical_gbs": round(logical / (ms * 1e-3) / 1e9, 1),
             "logical_frac_of_measured_peak": round(logical / (ms * 1e-3) / 1e9 / hbm, 4),
             "unique_kv_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
-            "note": "logical bytes count shared prefix blocks once per sample (L2 serves the "
-                    "repeats); unique bytes count each physical block once"}
+            "note": "logical bytes count shared blocks once per sequence that reads them (L2 "
+                    "serves the repeats); unique bytes count each physical block once"}
+
+
+def prefix_sharing_steps(pkv, W, device, prompt_len, steps=256):
+    """Decode steps of the prefix-sharing scenario (16 prompts x 8 samples)."""
+    sc = W.PrefixSharingScenario(prompt_len=prompt_len, decode_steps=steps)
+    res = scenario_steps(pkv, device, sc, steps, sc.unique_blocks_in_use)
+    return {"workload": f"16 prompts x {prompt_len} tokens x 8 samples, {steps} decode steps, "
+                        "block 32, 32 q / 8 kv heads, bf16", **res}
+
+
+def beam_search_steps(pkv, W, device, prompt_len=2048, width=16, steps=128):
+    """Decode steps of beam search over one prompt: every step a seeded number
+    of beams is dropped and a survivor forked in their place, sharing all of
+    its blocks; a beam whose last block is shared copies it before writing."""
+    sc = W.BeamSearchScenario(prompt_len=prompt_len, width=width, decode_steps=steps)
+    res = scenario_steps(pkv, device, sc, steps,
+                         lambda: int((sc.manager.refcount > 0).sum()))
+    return {"workload": f"beam search over one {prompt_len}-token prompt, {width} beams, "
+                        f"{steps} decode steps, block 16, 32 q / 8 kv heads, bf16",
+            **res, "mean_block_saving": round(float(sum(sc.savings) / len(sc.savings)), 4)}
 
 
 def swap_throughput(pkv, W, device, victims=16, reps=20):
@@ -618,6 +641,7 @@ def other_workloads(pkv, W, device, all_configs):
         extra["writes_and_copies"] = writes_throughput(pkv, W, device)
         extra["prefix_sharing"] = prefix_sharing_steps(pkv, W, device, 1024)
         extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
+        extra["beam_search"] = beam_search_steps(pkv, W, device)
     return extra
 
 
@@ -678,6 +702,8 @@ def single_workload(pkv, W, device, name):
         return swap_throughput(pkv, W, device)
     if name == "writes":
         return writes_throughput(pkv, W, device)
+    if name == "beam_search":
+        return beam_search_steps(pkv, W, device)
     return prefix_sharing_steps(pkv, W, device, 1040 if name == "prefix_sharing_cow" else 1024)
 
 

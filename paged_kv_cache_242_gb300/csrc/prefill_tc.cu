@@ -110,8 +110,19 @@ struct alignas(8) TcControl {
     int32_t valid[kStages];
 };
 
-constexpr size_t kSmemBytes = 1024 + kCtlOff + sizeof(TcControl);
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// Each sequence's number of row items, cached in shared memory so that dead
+// items of the work list are skipped without global loads (up to
+// kCachedSeqs sequences with fewer than 2^16 row items each).
+constexpr int kCachedSeqs = 4096;
+constexpr int kRowItemsOff = (kCtlOff + static_cast<int>(sizeof(TcControl)) + 15) / 16 * 16;
+constexpr size_t kSmemMaxBytes = 1024 + kRowItemsOff + kCachedSeqs * sizeof(uint16_t);
+static_assert(kSmemMaxBytes <= 232448, "shared memory per CTA");
+
+// Dynamic shared memory of a launch: the cache holds this call's sequences.
+inline size_t smem_bytes(int num_seqs) {
+    const int cached = num_seqs <= kCachedSeqs ? num_seqs : 0;
+    return 1024 + kRowItemsOff + static_cast<size_t>(cached) * sizeof(uint16_t);
+}
 
 // K tiles and Q tiles are K-major operands (64 dims per 128-byte row; k-step
 // ks starts in half ks / 4 at byte (ks % 4) * 32); V tiles are the MN-major B
@@ -130,12 +141,24 @@ struct Item {
     int first_lim[2];  // the smallest causal limit among the tile's rows
 };
 
-__device__ __forceinline__ bool load_item(const PrefillArgs& a, int64_t v, Item& it) {
+// The row items of sequence s: ceil(q_len * group / 256), 0 when its lengths
+// are invalid.
+__device__ __forceinline__ int seq_row_items(const PrefillArgs& a, int s) {
+    const int q_len = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+    const int n = __ldg(a.seq_lens + s);
+    if (n < 0 || n > a.max_seq_len || q_len < 0 || q_len > a.max_q_len || q_len > n) return 0;
+    return static_cast<int>((static_cast<int64_t>(q_len) * a.group + kItemRows - 1) / kItemRows);
+}
+
+// `cache`: the shared-memory copy of seq_row_items, or null.
+__device__ __forceinline__ bool load_item(const PrefillArgs& a, int64_t v, Item& it,
+                                          const uint16_t* cache) {
     const int H = a.num_kv_heads;
     const int64_t hs = v % (static_cast<int64_t>(H) * a.num_seqs);
     const int x = static_cast<int>(v / (static_cast<int64_t>(H) * a.num_seqs));
     it.s = static_cast<int>(hs / H);
     it.h = static_cast<int>(hs - static_cast<int64_t>(it.s) * H);
+    if (cache != nullptr && x >= cache[it.s]) return false;  // dead: no global loads
     it.q0 = __ldg(a.cu_q + it.s);
     const int q_len = __ldg(a.cu_q + it.s + 1) - it.q0;
     it.n = __ldg(a.seq_lens + it.s);
@@ -203,6 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&ctl->mma_done[1]), 1);
         fence_barrier_init();
     }
+    // every CTA caches the row items of every sequence (when they fit)
+    uint16_t* row_items_smem = reinterpret_cast<uint16_t*>(sm + kRowItemsOff);
+    const uint16_t* row_items = (a.num_seqs <= kCachedSeqs && X < 65536) ? row_items_smem : nullptr;
+    if (row_items != nullptr) {
+        for (int s = threadIdx.x; s < a.num_seqs; s += kThreads)
+            row_items_smem[s] = static_cast<uint16_t>(min(seq_row_items(a, s), 65535));
+    }
     // every sequence's lengths are checked once, spread over the grid
     for (int s = blockIdx.x * kThreads + threadIdx.x; s < a.num_seqs; s += gridDim.x * kThreads) {
         const int q_len = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
@@ -224,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool alive = true;
         for (int64_t v = blockIdx.x; alive && v < n_items; v += gridDim.x) {
             Item it;
-            if (!load_item(a, v, it)) continue;
+            if (!load_item(a, v, it, row_items)) continue;
             const int nblocks = (it.n + BS - 1) / BS;
             const int32_t* table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
             int win_base = -(1 << 30), win_id = -1;
@@ -359,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int64_t v = blockIdx.x; alive && v < n_items; v += gridDim.x) {
                 Item it;
-                if (!load_item(a, v, it)) continue;
+                if (!load_item(a, v, it, row_items)) continue;
                 flush();  // the previous item's last P V (its epilogue waits for it)
                 if (!alive) break;
                 const int n_t = q ? it.n_tiles[1] : it.n_tiles[0];
@@ -457,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         for (int64_t v = blockIdx.x; alive && v < n_items; v += gridDim.x) {
             Item it;
-            if (!load_item(a, v, it)) continue;
+            if (!load_item(a, v, it, row_items)) continue;
             J += it.n_keys;
             const int n_t = qt ? it.n_tiles[1] : it.n_tiles[0];
             const int first_lim = qt ? it.first_lim[1] : it.first_lim[0];
@@ -607,7 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename T, int BS>
 cudaError_t launch_tc_typed(const CUtensorMap& k_map, const CUtensorMap& v_map,
                             const PrefillArgs& a, cudaStream_t stream) {
-    cudaError_t err = ensure_smem_limit<paged_prefill_tc_kernel<T, BS>>(kSmemBytes);
+    const size_t smem = smem_bytes(a.num_seqs);
+    cudaError_t err = ensure_smem_limit<paged_prefill_tc_kernel<T, BS>>(smem);
     if (err != cudaSuccess) return err;
     const int64_t row_items = (static_cast<int64_t>(a.max_q_len) * a.group + kItemRows - 1) / kItemRows;
     const int X = static_cast<int>(row_items > 0 ? row_items : 1);
@@ -620,7 +651,7 @@ cudaError_t launch_tc_typed(const CUtensorMap& k_map, const CUtensorMap& v_map,
     // persistent: one CTA per SM walks the work list
     const int ctas = static_cast<int>(items < sms ? items : sms);
     return launch_pdl(paged_prefill_tc_kernel<T, BS>, dim3(ctas > 0 ? ctas : 1), dim3(kThreads),
-                      kSmemBytes, stream, k_map, v_map, a, X);
+                      smem, stream, k_map, v_map, a, X);
 }
 
 template <typename T>

@@ -91,6 +91,25 @@ def test_prefill_fp16_ragged(B):
     assert_attention_close(out, ref, f"prefill fp16 B={B}")
 
 
+def test_prefill_mixed_new_tokens_and_prompts():
+    """One call mixing 250 sequences that add one token after a cached context with three long
+    prompts: most of the persistent grid's work list is empty items, skipped from the
+    per-sequence cache in shared memory."""
+    g = torch.Generator().manual_seed(13)
+    S = 253
+    ctx = torch.randint(100, 600, (S,), generator=g).tolist()
+    ql = [1] * S
+    for i, x in ((7, 1500), (100, 700), (200, 1100)):
+        ctx[i], ql[i] = 0, x
+    step = W.build_prefill_step("mixed", ctx, ql, 32, 8, 16, "bfloat16", seed=13)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(step, err)
+    ref = _reference(step)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, "prefill mixed")
+
+
 def test_prefill_fp16_and_mqa():
     step = W.build_prefill_step("fp16", [300, 0], [129, 255], 8, 1, 16, "float16", seed=7)
     out, _ = _run(step)

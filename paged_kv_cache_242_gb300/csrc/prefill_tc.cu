@@ -74,6 +74,13 @@ constexpr float kRescaleLog2 = 8.f;
 template <typename T>
 constexpr int kPParts = std::is_same<T, __nv_bfloat16>::value ? 2 : 1;
 
+// max(a, b, c) in one instruction (sm_100+); a NaN input is ignored as in fmaxf.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Packed two-lane fp32 arithmetic (one sm_100+ .f32x2 instruction for a
 // pair; each lane rounds exactly as the scalar instruction does).
 __device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b) {
@@ -543,8 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x0 = key0 + i <= lim ? x0 : -INFINITY;  // also drops NaN
                         x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
                     }
-                    mx[i & 3] = fmaxf(mx[i & 3], x0);
-                    mx[(i + 1) & 3] = fmaxf(mx[(i + 1) & 3], x1);
+                    mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], x0, x1);
                 }
                 const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 // lazy rescale: keep the older max until the row max exceeds it by 2^8

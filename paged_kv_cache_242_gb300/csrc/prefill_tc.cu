@@ -32,11 +32,12 @@
 //              softmax;
 //   warps 3-6  softmax of Q tile A, warps 7-10 of Q tile B, one thread per row
 //              (one TMEM lane): read the row's 64 scores of S from TMEM,
-//              scale, causal mask, max, weights, write P's two parts over
-//              those TMEM columns, and rescale the O row in TMEM when the max
-//              has grown by more than 2^8 (until then the weights are taken
-//              against the older, smaller max, which only lets them exceed 1);
-//              at the end of the item write O / l.
+//              scale, causal mask, weights, write P's parts over
+//              those TMEM columns.  Once the row has a finite running max the
+//              weights are taken against it without a max pass; a tile whose
+//              weights would sum past kMaxTileSum moves the max (by the scores'
+//              max, when it has grown by more than 2^8) and rescales the O row
+//              in TMEM and the sum.  At the end of the item write O / l.
 // While one Q tile's softmax runs, the tensor cores work on the other's S or
 // P V and on the next S of the same tile (two S / P buffers per tile).
 //
@@ -73,6 +74,12 @@ constexpr float kRescaleLog2 = 8.f;
 // part and the low part of the remainder; binary16 keeps 11 and goes whole.
 template <typename T>
 constexpr int kPParts = std::is_same<T, __nv_bfloat16>::value ? 2 : 1;
+
+// The largest sum of a tile's weights taken against a stale running max
+// before the max is moved: weights stay well inside the 16-bit type's range
+// (bf16: 2^127; binary16: 65504).
+template <typename T>
+constexpr float kMaxTileSum = std::is_same<T, __nv_bfloat16>::value ? 4294967296.f : 32768.f;
 
 // max(a, b, c) in one instruction (sm_100+); a NaN input is ignored as in fmaxf.
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -541,63 +548,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(sp_addr, *reinterpret_cast<uint32_t(*)[32]>(v));
                 tmem_ld32(sp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                 tmem_ld_wait();
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int i = 0; i < 64; i += 2) {
-                    float x0, x1;
-                    mul2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl);
-                    if (masked) {
-                        x0 = key0 + i <= lim ? x0 : -INFINITY;  // also drops NaN
-                        x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
-                    }
-                    mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], x0, x1);
-                }
-                const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                // lazy rescale: keep the older max until the row max exceeds it by 2^8
-                const float m_new = fmaxf(m_used, row_max);
-                const bool bump = m_new > m_used + kRescaleLog2;  // true at the first finite max
-                const float m_tgt = bump ? m_new : m_used;
-                const float base = m_tgt == -INFINITY ? 0.f : m_tgt;
-                const float alpha = bump ? ex2(m_used - base) : 1.f;  // 0 while m_used = -inf
-                m_used = m_tgt;
-
-                if (j >= 1 && __any_sync(0xffffffffu, bump)) {
-                    // O must hold the previous tile's P V before it is rescaled
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(smem_addr(&ctl->o_done[qt][(Tt - 1) & 1]),
-                                              ((Tt - 1) >> 1) & 1))) {
-                        alive = false;
-                        break;
-                    }
-                    tcgen05_after_sync();
-#pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint32_t ov[32];
-                        const uint32_t o_addr = tbase + kOCol + 32 * c4;
-                        tmem_ld32(o_addr, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(o_addr, ov);
-                    }
-                    tmem_st_wait();
-                }
-                // ---- weights, their sum, P's high / low parts over these columns ----
+                // ---- weights against the running max, and their sum ----
+                // Once a row has a finite max, its weights are taken against it
+                // without a max pass: they stay exact in fp32, and P keeps the same
+                // relative precision at any size.  Only a tile whose weights sum past
+                // kMaxTileSum (or a row without a finite max yet) takes the pass
+                // below, which moves the max and rescales O and the sum.
                 float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                auto weights = [&](float base) {
 #pragma unroll
-                for (int i = 0; i < 64; i += 2) {
-                    float x0, x1;
-                    fma2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl, -base);
-                    if (masked) {
-                        x0 = key0 + i <= lim ? x0 : -INFINITY;
-                        x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
+                    for (int k = 0; k < 4; ++k) ps[k] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 64; i += 2) {
+                        float x0, x1;
+                        fma2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl, -base);
+                        if (masked) {
+                            x0 = key0 + i <= lim ? x0 : -INFINITY;
+                            x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
+                        }
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        const int a2 = (i >> 1) & 1;
+                        add2(ps[2 * a2], ps[2 * a2 + 1], ps[2 * a2], ps[2 * a2 + 1], p0, p1);
+                        v[i] = __float_as_uint(p0);
+                        v[i + 1] = __float_as_uint(p1);
                     }
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    const int a2 = (i >> 1) & 1;
-                    add2(ps[2 * a2], ps[2 * a2 + 1], ps[2 * a2], ps[2 * a2 + 1], p0, p1);
-                    v[i] = __float_as_uint(p0);
-                    v[i + 1] = __float_as_uint(p1);
+                };
+                float alpha = 1.f;
+                bool need_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+                if (!need_max) {
+                    weights(m_used);
+                    const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                    need_max = __any_sync(0xffffffffu, !(sum <= kMaxTileSum<T>));
+                    if (need_max) {  // the scores again, for the pass below
+                        tmem_ld32(sp_addr, *reinterpret_cast<uint32_t(*)[32]>(v));
+                        tmem_ld32(sp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                        tmem_ld_wait();
+                    }
+                }
+                if (need_max) {
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int i = 0; i < 64; i += 2) {
+                        float x0, x1;
+                        mul2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl);
+                        if (masked) {
+                            x0 = key0 + i <= lim ? x0 : -INFINITY;  // also drops NaN
+                            x1 = key0 + i + 1 <= lim ? x1 : -INFINITY;
+                        }
+                        mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], x0, x1);
+                    }
+                    const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    // lazy rescale: keep the older max until the row max exceeds it by 2^8
+                    const float m_new = fmaxf(m_used, row_max);
+                    const bool bump = m_new > m_used + kRescaleLog2;  // true at the first finite max
+                    const float m_tgt = bump ? m_new : m_used;
+                    const float base = m_tgt == -INFINITY ? 0.f : m_tgt;
+                    alpha = bump ? ex2(m_used - base) : 1.f;  // 0 while m_used = -inf
+                    m_used = m_tgt;
+                    if (j >= 1 && __any_sync(0xffffffffu, bump)) {
+                        // O must hold the previous tile's P V before it is rescaled
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(smem_addr(&ctl->o_done[qt][(Tt - 1) & 1]),
+                                                  ((Tt - 1) >> 1) & 1))) {
+                            alive = false;
+                            break;
+                        }
+                        tcgen05_after_sync();
+#pragma unroll 1
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t ov[32];
+                            const uint32_t o_addr = tbase + kOCol + 32 * c4;
+                            tmem_ld32(o_addr, ov);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                            tmem_st32(o_addr, ov);
+                        }
+                        tmem_st_wait();
+                    }
+                    weights(base);
                 }
                 uint32_t pw[32];
 #pragma unroll

@@ -110,6 +110,24 @@ def test_prefill_mixed_new_tokens_and_prompts():
     assert_attention_close(out, ref, "prefill mixed")
 
 
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+def test_prefill_growing_scores(dtype):
+    """Keys whose norms grow along the prompt, so later key tiles score far above earlier ones
+    (log2 score ranges of ~100): the running max must move, O and the sums must be rescaled,
+    and no weight may overflow the 16-bit type."""
+    step = W.build_prefill_step("grow", [0, 0, 300], [700, 130, 400], 32, 8, 16, dtype, seed=14)
+    T = step.k_new.shape[0]
+    growth = (1.0 + torch.arange(T, dtype=torch.float32) / 8.0).view(T, 1, 1)
+    step.k_new.copy_((step.k_new.float() * growth).to(step.k_new.dtype))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(step, err)
+    ref = _reference(step)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    assert_attention_close(out, ref, f"prefill growing scores {dtype}")
+
+
 def test_prefill_fp16_and_mqa():
     step = W.build_prefill_step("fp16", [300, 0], [129, 255], 8, 1, 16, "float16", seed=7)
     out, _ = _run(step)

@@ -24,7 +24,8 @@ produces the kernels' inputs; ``workloads`` generates seeded synthetic
 decode batches.
 """
 from ._lib import PKVError  # noqa: F401
-from .ops import (cache_desc, copy_blocks, copy_blocks_layers,  # noqa: F401
+from .ops import (DecodeAttentionPlan, KVWritePlan, cache_desc,  # noqa: F401
+                  copy_blocks, copy_blocks_layers,
                   decode_partition_size, decode_workspace_bytes, kv_write, kv_write_layers,
                   kv_write_fp8, paged_decode_attention, paged_decode_attention_fp8,
                   paged_prefill_attention, swap_blocks)
@@ -32,4 +33,4 @@ from .ops import (cache_desc, copy_blocks, copy_blocks_layers,  # noqa: F401
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
            "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
            "copy_blocks_layers", "paged_prefill_attention", "kv_write_fp8",
-           "paged_decode_attention_fp8"]
+           "paged_decode_attention_fp8", "KVWritePlan", "DecodeAttentionPlan"]

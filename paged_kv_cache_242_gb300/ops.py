@@ -57,10 +57,7 @@ def _err_ptr(err_flag: Optional[torch.Tensor]) -> Optional[int]:
     return err_flag.data_ptr()
 
 
-def kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
-             k_cache: torch.Tensor, v_cache: torch.Tensor,
-             err_flag: Optional[torch.Tensor] = None) -> None:
-    """Write k, v [T, H_kv, d] into the caches at ``slot_mapping`` (int64 [T])."""
+def _check_kv_write(k, v, slot_mapping, k_cache, v_cache):
     _check_caches(k_cache, v_cache)
     desc = cache_desc(k_cache)
     T = int(slot_mapping.numel())
@@ -71,6 +68,14 @@ def kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     _require(k.dtype == k_cache.dtype and v.dtype == k_cache.dtype, "k/v dtype must match the cache")
     _require(k.is_contiguous() and v.is_contiguous() and k.is_cuda and v.is_cuda,
              "k and v must be contiguous CUDA tensors")
+    return desc, T
+
+
+def kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor,
+             err_flag: Optional[torch.Tensor] = None) -> None:
+    """Write k, v [T, H_kv, d] into the caches at ``slot_mapping`` (int64 [T])."""
+    desc, T = _check_kv_write(k, v, slot_mapping, k_cache, v_cache)
     lib = _lib.load()
     _lib.check(lib.pkv_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache),
                                 _ptr(v_cache), desc, _err_ptr(err_flag), _stream(k_cache.device)),
@@ -89,6 +94,23 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, max_seq_len: int, bl
                                                        int(block_size), int(partition_size)))
 
 
+def _check_decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads):
+    _check_caches(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    if num_kv_heads is not None:
+        _require(int(num_kv_heads) == desc.num_kv_heads, "num_kv_heads disagrees with the cache")
+    _require(q.dim() == 3 and q.shape[2] == desc.head_dim, "q must be [num_seqs, num_q_heads, d]")
+    _require(q.dtype == k_cache.dtype and q.is_cuda and q.is_contiguous(),
+             "q must be a contiguous CUDA tensor of the cache dtype")
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
+             block_tables.shape[0] == S and block_tables.is_contiguous() and block_tables.is_cuda,
+             "block_tables must be a contiguous CUDA int32 [num_seqs, max_blocks] tensor")
+    _require(seq_lens.dtype == torch.int32 and seq_lens.numel() == S and seq_lens.is_cuda and
+             seq_lens.is_contiguous(), "seq_lens must be a contiguous CUDA int32 [num_seqs] tensor")
+    return desc, S, Hq
+
+
 def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            block_tables: torch.Tensor, seq_lens: torch.Tensor,
                            num_kv_heads: Optional[int] = None, scale: Optional[float] = None,
@@ -104,19 +126,7 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     ``workspace`` (uint8 CUDA tensor, zero-filled when new) is allocated
     when needed and omitted; reuse one across calls to avoid allocations.
     """
-    _check_caches(k_cache, v_cache)
-    desc = cache_desc(k_cache)
-    if num_kv_heads is not None:
-        _require(int(num_kv_heads) == desc.num_kv_heads, "num_kv_heads disagrees with the cache")
-    _require(q.dim() == 3 and q.shape[2] == desc.head_dim, "q must be [num_seqs, num_q_heads, d]")
-    _require(q.dtype == k_cache.dtype and q.is_cuda and q.is_contiguous(),
-             "q must be a contiguous CUDA tensor of the cache dtype")
-    S, Hq = int(q.shape[0]), int(q.shape[1])
-    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and
-             block_tables.shape[0] == S and block_tables.is_contiguous() and block_tables.is_cuda,
-             "block_tables must be a contiguous CUDA int32 [num_seqs, max_blocks] tensor")
-    _require(seq_lens.dtype == torch.int32 and seq_lens.numel() == S and seq_lens.is_cuda and
-             seq_lens.is_contiguous(), "seq_lens must be a contiguous CUDA int32 [num_seqs] tensor")
+    desc, S, Hq = _check_decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads)
     if scale is None:
         scale = desc.head_dim ** -0.5
     if max_seq_len is None:
@@ -358,7 +368,67 @@ def copy_blocks_layers(k_caches, v_caches, src_dst_pairs: torch.Tensor,
                "pkv_copy_blocks_layers")
 
 
+class KVWritePlan:
+    """kv_write validated and marshalled once for a fixed set of tensors.
+
+    A serving loop writes each step's new keys / values through the same
+    tensors (their contents change, their storage does not); ``run()`` then
+    issues the C call directly, without re-checking shapes and dtypes.  The
+    tensors must stay alive and in place while the plan is used."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 err_flag: Optional[torch.Tensor] = None) -> None:
+        desc, T = _check_kv_write(k, v, slot_mapping, k_cache, v_cache)
+        self._tensors = (k, v, slot_mapping, k_cache, v_cache, err_flag)  # kept alive
+        self._device = k_cache.device
+        self._args = (_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache), desc,
+                      _err_ptr(err_flag))
+        self._fn = _lib.load().pkv_kv_write
+
+    def run(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        s = (stream or torch.cuda.current_stream(self._device)).cuda_stream
+        _lib.check(self._fn(*self._args, s), "pkv_kv_write")
+
+
+class DecodeAttentionPlan:
+    """paged_decode_attention validated and marshalled once for a fixed set of
+    tensors (q, caches, block tables, lengths, out, workspace), as KVWritePlan.
+    ``max_seq_len`` is fixed by the plan: every later seq_lens must stay at or
+    below it (a longer one sets PKV_DEVERR_BAD_SEQ_LEN and is skipped)."""
+
+    def __init__(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, *,
+                 max_seq_len: int, num_kv_heads: Optional[int] = None,
+                 scale: Optional[float] = None, partition_size: int = 0,
+                 workspace: Optional[torch.Tensor] = None,
+                 err_flag: Optional[torch.Tensor] = None) -> None:
+        desc, S, Hq = _check_decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads)
+        _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous() and
+                 out.is_cuda, "out must match q")
+        need = decode_workspace_bytes(S, Hq, max_seq_len, desc.block_size, partition_size,
+                                      desc.head_dim)
+        if workspace is None:
+            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
+        _require(workspace.numel() * workspace.element_size() >= need, "workspace too small")
+        if scale is None:
+            scale = desc.head_dim ** -0.5
+        self._tensors = (q, k_cache, v_cache, block_tables, seq_lens, out, workspace, err_flag)
+        self._device = q.device
+        self._args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                      int(block_tables.shape[1]), _ptr(seq_lens), int(max_seq_len), S, Hq, desc,
+                      ctypes.c_float(float(scale)), int(partition_size), _ptr(workspace),
+                      workspace.numel() * workspace.element_size(), _ptr(out), _err_ptr(err_flag))
+        self._fn = _lib.load().pkv_paged_decode_attention
+        self.out = out
+
+    def run(self, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        s = (stream or torch.cuda.current_stream(self._device)).cuda_stream
+        _lib.check(self._fn(*self._args, s), "pkv_paged_decode_attention")
+        return self.out
+
+
 __all__ = ["kv_write", "paged_decode_attention", "copy_blocks", "decode_workspace_bytes",
            "decode_partition_size", "cache_desc", "PKVError", "swap_blocks", "kv_write_layers",
            "copy_blocks_layers", "paged_prefill_attention", "kv_write_fp8",
-           "paged_decode_attention_fp8"]
+           "paged_decode_attention_fp8", "KVWritePlan", "DecodeAttentionPlan"]

@@ -312,6 +312,46 @@ def test_stream_workspace_reuse_with_leftover_contents():
         assert_attention_close(out, ref, "reused workspace")
 
 
+def test_plans_match_the_calls():
+    """KVWritePlan / DecodeAttentionPlan, validated once and run repeatedly on the same tensors
+    whose contents change, give the same bits as the plain calls."""
+    step = _custom([2500, 3000, 700, 1], 32, 8, 16, "bfloat16", seed=44)
+    kc, vc = bits(step.k_cache), bits(step.v_cache)
+    ref, _, _ = oracle_step(step, kc, vc)
+    dev = to_device(step)
+    plain = {k: v.clone() for k, v in dev.items()}
+    pkv.kv_write(plain["k_new"], plain["v_new"], plain["slot_mapping"], plain["k_cache"],
+                 plain["v_cache"])
+    want = pkv.paged_decode_attention(plain["q"], plain["k_cache"], plain["v_cache"],
+                                      plain["block_tables"], plain["seq_lens"], step.num_kv_heads,
+                                      step.scale, max_seq_len=step.max_seq_len)
+    out = torch.empty_like(dev["q"])
+    write = pkv.KVWritePlan(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"],
+                            dev["v_cache"])
+    attend = pkv.DecodeAttentionPlan(dev["q"], dev["k_cache"], dev["v_cache"],
+                                     dev["block_tables"], dev["seq_lens"], out,
+                                     max_seq_len=step.max_seq_len, num_kv_heads=step.num_kv_heads,
+                                     scale=step.scale)
+    side = torch.cuda.Stream()
+    for stream in (None, side):
+        out.zero_()
+        torch.cuda.synchronize()
+        write.run(stream)
+        got = attend.run(stream)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+        assert_attention_close(got, ref, "plan")
+    # new contents in the same tensors: the plan sees them
+    q2 = torch.randn(dev["q"].shape, generator=torch.Generator().manual_seed(3)).to(dev["q"].dtype)
+    dev["q"].copy_(q2.cuda())
+    want2 = pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                       dev["block_tables"], dev["seq_lens"], step.num_kv_heads,
+                                       step.scale, max_seq_len=step.max_seq_len)
+    got2 = attend.run()
+    torch.cuda.synchronize()
+    assert torch.equal(got2, want2)
+
+
 def test_cuda_graph_replay():
     """A captured attention call replays correctly."""
     step = _custom([2500, 3000, 700], 32, 8, 16, "bfloat16", seed=42)

@@ -128,6 +128,25 @@ def test_prefill_growing_scores(dtype):
     assert_attention_close(out, ref, f"prefill growing scores {dtype}")
 
 
+@pytest.mark.parametrize("heads", [(64, 1), (128, 2)])
+def test_prefill_large_groups(heads):
+    """Groups of 64 query heads per KV head, the largest supported: a 128-row Q tile is two
+    tokens.  A group of 128 is refused with PKV_ERR_UNSUPPORTED."""
+    H_q, H_kv = heads
+    too_big = W.build_prefill_step("g128", [0], [3], 128, 1, 16, "bfloat16", seed=15)
+    with pytest.raises(pkv.PKVError) as e:
+        _run(too_big)
+    assert e.value.status == 2
+    step = W.build_prefill_step("groups", [0, 37, 200], [41, 9, 30], H_q, H_kv, 16, "bfloat16",
+                                seed=15 + H_q + H_kv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(step, err)
+    ref = _reference(step)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, f"prefill heads={heads}")
+
+
 def test_prefill_fp16_and_mqa():
     step = W.build_prefill_step("fp16", [300, 0], [129, 255], 8, 1, 16, "float16", seed=7)
     out, _ = _run(step)

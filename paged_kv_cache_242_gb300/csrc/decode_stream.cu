@@ -28,8 +28,7 @@ size_t stream_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads_or
         rows = warps * gmax + static_cast<size_t>(num_seqs) * num_q_heads;
     }
     const size_t floats = rows * (kHeadDim + 2);
-    const size_t prefix = (static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t);
-    return floats * sizeof(float) + ((prefix + 255) / 256) * 256;
+    return floats * sizeof(float);
 }
 
 cudaError_t launch_paged_decode_stream(const CUtensorMap& k_map16, const CUtensorMap& v_map16,

@@ -38,8 +38,7 @@
 // domain, mma.sync P V.
 //
 // The prologue of every CTA scans the sequence lengths into a prefix of tile
-// counts held in shared memory (up to 4096 sequences); CTA 0 also stores it
-// in the workspace for the merge kernel.
+// counts held in shared memory (up to 4096 sequences).
 #pragma once
 
 #include "decode_policy.cuh"
@@ -182,9 +181,6 @@ __global__ void __launch_bounds__(Policy::kWarps * 32, 1)
             prefix[S] = total;
         }
         __syncthreads();
-        if (blockIdx.x == 0) {
-            for (int idx = threadIdx.x; idx <= S; idx += kThreads) a.ws_prefix[idx] = prefix[idx];
-        }
     }
 
     // ---- this warp's share of the tiles --------------------------------------
@@ -319,36 +315,56 @@ __global__ void __launch_bounds__(Policy::kWarps * 32, 1)
 // Merge of the partial statistics of segments cut by warp ranges (Eq. 4):
 // out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w, M = max_w m_w.
 // One warp per (segment, query head of the group), four output columns per
-// lane.  After one round trip for the segment's position, the (m, l, acc)
-// of up to eight pieces are loaded together and folded in with the running
-// max / sum, so a segment of up to eight pieces costs two dependent memory
-// round trips.  Launched with programmatic dependent launch: its CTAs wait
-// for the streaming kernel and start as soon as it finishes.
+// lane.  Launched with programmatic dependent launch, its CTAs start while the
+// streaming kernel runs: each warp first derives its segment's position (the
+// tile prefix of its sequence and the total) from the sequence lengths, which
+// are inputs complete before the streaming kernel started, then waits for the
+// streaming kernel.  After that the (m, l, acc) of up to eight pieces are
+// loaded together and folded in with the running max / sum, so a segment of
+// up to eight pieces costs one dependent memory round trip.
 constexpr int kMergeWarps = 4;
 constexpr int kMergeBatch = 8;
 
-template <typename T>
+template <typename T, int kTT>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const DecodeArgs a) {
-    pdl_wait_prerequisites();
-    pdl_allow_dependents();
     const int g = a.group;
     const int H = a.num_kv_heads;
+    const int S = a.num_seqs;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
-    if (item >= static_cast<int64_t>(a.num_seqs) * H * g) return;
+    if (item >= static_cast<int64_t>(S) * H * g) return;
     const int lane = threadIdx.x & 31;
     const int r = static_cast<int>(item % g);
     const int64_t j = item / g;  // segment = s * H + h
     const int s = static_cast<int>(j / H);
     const int h = static_cast<int>(j - static_cast<int64_t>(s) * H);
-    const int p_s = a.ws_prefix[s];
-    const int nt = a.ws_prefix[s + 1] - p_s;
-    const int64_t total_tiles = static_cast<int64_t>(a.ws_prefix[a.num_seqs]) * H;
-    uint2* ocol = reinterpret_cast<uint2*>(
+    // tiles before sequence s, of sequence s, and in all (the streaming kernel's prefix)
+    int before = 0, mine = 0, total = 0;
+    for (int base = 0; base < S; base += 32) {
+        const int idx = base + lane;
+        const int t = idx < S ? (clamped_len(a, idx, false) + kTT - 1) / kTT : 0;
+        total += t;
+        before += idx < s ? t : 0;
+        mine += idx == s ? t : 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        total += __shfl_xor_sync(0xffffffffu, total, off);
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+        mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    }
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
+    const int p_s = before;
+    const int nt = mine;
+    const int64_t total_tiles = static_cast<int64_t>(total) * H;
+    // 32-bit stores: out is only 4-byte aligned
+    uint32_t* ocol = reinterpret_cast<uint32_t*>(
         static_cast<T*>(a.out) +
         (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g + r) * kHeadDim +
         lane * 4);
     if (nt == 0) {  // empty sequence: zero output
-        *ocol = make_uint2(0u, 0u);
+        ocol[0] = 0u;
+        ocol[1] = 0u;
         return;
     }
     const int64_t per = (total_tiles + a.num_warps - 1) / a.num_warps;
@@ -388,7 +404,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
         }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    *ocol = make_uint2(Mma<T>::pack(acc.x * inv, acc.y * inv), Mma<T>::pack(acc.z * inv, acc.w * inv));
+    ocol[0] = Mma<T>::pack(acc.x * inv, acc.y * inv);
+    ocol[1] = Mma<T>::pack(acc.z * inv, acc.w * inv);
 }
 
 template <bool kFp8, int kWarps>
@@ -411,7 +428,8 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
     if (err != cudaSuccess) return err;
     const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.group;
     const int64_t blocks = (items + kMergeWarps - 1) / kMergeWarps;
-    return launch_pdl(merge_stream_kernel<T>, dim3(static_cast<unsigned>(blocks)),
+    return launch_pdl(merge_stream_kernel<T, StreamLayout<kFp8, Policy::kWarps>::kTileTokens>,
+                      dim3(static_cast<unsigned>(blocks)),
                       dim3(kMergeWarps * 32), 0, stream, a);
 }
 
@@ -451,13 +469,12 @@ cudaError_t launch_stream(const CUtensorMap& k_map, const CUtensorMap& v_map, De
     if (ctas > cap) ctas = cap;
     if (ctas < 1) ctas = 1;
     a.num_warps = static_cast<int32_t>(ctas) * kWarps;
-    // workspace layout: acc [rows][128], m [rows], l [rows], prefix [S + 1]
+    // workspace layout: acc [rows][128], m [rows], l [rows]
     const size_t rows = (static_cast<size_t>(a.num_warps) +
                          static_cast<size_t>(a.num_seqs) * a.num_kv_heads) * a.group;
     float* ws = a.ws_acc;
     a.ws_m = ws + rows * kHeadDim;
     a.ws_l = a.ws_m + rows;
-    a.ws_prefix = reinterpret_cast<int32_t*>(a.ws_l + rows);
     return dtype == PKV_BF16
                ? launch_stream_block<Policy<__nv_bfloat16>>(k_map, v_map, a, block_size, (int)ctas,
                                                             stream)

@@ -81,7 +81,6 @@ struct DecodeArgs {
     int32_t max_partitions;     // ceil(max_seq_len / partition_size), >= 1
     int32_t max_seq_len;
     float scale_log2;           // softmax scale * log2(e) (* k_scale for 8-bit pools)
-    int32_t* ws_prefix;         // stream mode: [S + 1] tile prefix over sequences
     int32_t num_warps;          // stream mode: warps in the grid
     float v_scale;              // 8-bit pools: value scale (1 otherwise)
 };

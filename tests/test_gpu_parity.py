@@ -312,6 +312,29 @@ def test_stream_workspace_reuse_with_leftover_contents():
         assert_attention_close(out, ref, "reused workspace")
 
 
+def test_four_byte_aligned_q_and_out():
+    """The 16-bit entry point accepts q and out aligned to only 4 bytes: views 4 bytes into
+    larger buffers give the same bits as aligned tensors (cut segments included)."""
+    step = _custom([2500, 3000, 700, 0, 1], 32, 8, 16, "bfloat16", seed=45)
+    dev = to_device(step)
+    pkv.kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], dev["k_cache"], dev["v_cache"])
+    want = pkv.paged_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                      dev["block_tables"], dev["seq_lens"], step.num_kv_heads,
+                                      step.scale, max_seq_len=step.max_seq_len)
+    n = dev["q"].numel()
+    qbuf = torch.empty(n + 2, dtype=dev["q"].dtype, device="cuda")
+    obuf = torch.full((n + 2,), float("nan"), dtype=dev["q"].dtype, device="cuda")
+    q4 = qbuf[2:].view(dev["q"].shape)  # 4 bytes past a 256-byte boundary
+    out4 = obuf[2:].view(dev["q"].shape)
+    assert q4.data_ptr() % 8 == 4 and out4.data_ptr() % 8 == 4
+    q4.copy_(dev["q"])
+    pkv.paged_decode_attention(q4, dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                               dev["seq_lens"], step.num_kv_heads, step.scale, out4,
+                               max_seq_len=step.max_seq_len)
+    torch.cuda.synchronize()
+    assert torch.equal(out4, want)
+
+
 def test_plans_match_the_calls():
     """KVWritePlan / DecodeAttentionPlan, validated once and run repeatedly on the same tensors
     whose contents change, give the same bits as the plain calls."""

@@ -89,7 +89,11 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 // Packed two-lane fp32 arithmetic (one sm_100+ .f32x2 instruction for a
-// pair; each lane rounds exactly as the scalar instruction does).
+// pair).  A packed multiply whose result feeds a packed add or subtract may be
+// evaluated as one fused operation, without the product's rounding, so they
+// are used only where no multiply feeds an add: the scale before the max, the
+// exponent argument (an explicit fma), the sums of weights and the low part
+// of P (a subtract of unpacked values).
 __device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b) {
     asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
         "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
@@ -121,7 +125,6 @@ struct alignas(8) TcControl {
     uint64_t o_done[2][2];  // P V of that buffer completed: O current, buffer free
     uint64_t mma_done[2];   // [issuer]
     uint32_t tmem_base;
-    int32_t valid[kStages];
 };
 
 // Each sequence's number of row items, cached in shared memory so that dead
@@ -304,7 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t full = smem_addr(&ctl->kv_full[st]);
-                    ctl->valid[st] = ok ? 1 : 0;
                     if (ok) {
                         const uint32_t kb = s_base + st * 2 * kTile;
                         const uint32_t vb = kb + kTile;

@@ -46,7 +46,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 SINGLE_WORKLOADS = ("tiny", "opt13b_like", "long_context", "long_context_fp8", "prefix_sharing",
-                    "prefix_sharing_cow", "swap", "writes", "beam_search")
+                    "prefix_sharing_cow", "swap", "writes", "beam_search", "decode_shapes")
 
 
 def parse_args():
@@ -648,6 +648,7 @@ def other_workloads(pkv, W, device, all_configs):
         extra["prefix_sharing"] = prefix_sharing_steps(pkv, W, device, 1024)
         extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
         extra["beam_search"] = beam_search_steps(pkv, W, device)
+        extra["decode_shapes"] = decode_shapes(pkv, W, device)
     return extra
 
 
@@ -687,6 +688,23 @@ def writes_throughput(pkv, W, device, n_pairs=2000):
     return res
 
 
+# (sequences, tokens each): from one sequence to a few dozen, 32 q / 8 kv heads
+DECODE_SHAPES = ((1, 2048), (4, 4096), (1, 32768), (16, 2048), (32, 1024))
+
+
+def decode_shapes(pkv, W, device):
+    """Equal-length decode batches with few (sequence, KV head) segments, each
+    cut over many warps of the streaming grid."""
+    res = {}
+    for i, (S, n) in enumerate(DECODE_SHAPES):
+        st = W.build_decode_step("shape", [n - 1] * S, 32, 8, 16, "bfloat16", seed=90 + i,
+                                 pool_factor=1.0)
+        res[f"S{S}_n{n}"] = measure_attention(
+            pkv, st, device, "shape", f"{S} x {n} tokens, 32 q / 8 kv heads, bf16, block 16")
+        del st
+    return res
+
+
 def single_workload(pkv, W, device, name):
     """One workload's decode attention (or full prefix-sharing steps) measured alone."""
     if name == "tiny":
@@ -710,6 +728,8 @@ def single_workload(pkv, W, device, name):
         return writes_throughput(pkv, W, device)
     if name == "beam_search":
         return beam_search_steps(pkv, W, device)
+    if name == "decode_shapes":
+        return decode_shapes(pkv, W, device)
     return prefix_sharing_steps(pkv, W, device, 1040 if name == "prefix_sharing_cow" else 1024)
 
 

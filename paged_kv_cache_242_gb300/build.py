@@ -5,6 +5,11 @@
 Each translation unit compiles in parallel, then the objects link into
 ``paged_kv_cache_242_gb300/_build/libpkv.so`` with the CUDA runtime linked
 statically and only the ``pkv_*`` symbols exported.
+
+``PKV_NVCC_EXTRA_FLAGS`` (space-separated) adds nvcc options, e.g. the
+``-DPKV_*`` tuning definitions of ``csrc/pkv_internal.h`` and
+``csrc/decode_stream.cuh``; a build with other flags than the last one
+recompiles everything.
 """
 from __future__ import annotations
 
@@ -43,8 +48,22 @@ def _inputs():
         os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "pkv.h")]
 
 
+def _flags():
+    return NVCC_FLAGS + os.environ.get("PKV_NVCC_EXTRA_FLAGS", "").split()
+
+
+def _flags_stamp():
+    return os.path.join(BUILD_DIR, "flags.txt")
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIBRARY):
+        return False
+    try:
+        with open(_flags_stamp()) as f:
+            if f.read() != " ".join(_flags()):
+                return False
+    except OSError:
         return False
     built = os.path.getmtime(LIBRARY)
     return all(os.path.getmtime(p) <= built for p in _inputs())
@@ -54,12 +73,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIBRARY
     nvcc = _nvcc()
+    flags = _flags()
     os.makedirs(BUILD_DIR, exist_ok=True)
     objects = []
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src).replace(".cu", ".o"))
-        cmd = [nvcc] + NVCC_FLAGS + ["-c", src, "-o", obj]
+        cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -81,6 +101,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
     os.replace(tmp, LIBRARY)
+    with open(_flags_stamp(), "w") as f:
+        f.write(" ".join(flags))
     return LIBRARY
 
 

@@ -322,15 +322,44 @@ __global__ void __launch_bounds__(Policy::kWarps * 32, 1)
 // streaming kernel.  After that the (m, l, acc) of up to eight pieces are
 // loaded together and folded in with the running max / sum, so a segment of
 // up to eight pieces costs one dependent memory round trip.
+//
+// Narrow form: kMergeWarps warps per CTA, one per (segment, query head).
+// Wide form, for grids with many warps per segment (long sequences, few
+// segments): one CTA of kMergeWideWarps warps per (segment,
+// query head); the warps take the batches of eight pieces in turn and their
+// (max, sum, acc) are combined through shared memory with the same rule.
 constexpr int kMergeWarps = 4;
+constexpr int kMergeWideWarps = 8;
+#ifndef PKV_MERGE_WIDE_PIECES
+#define PKV_MERGE_WIDE_PIECES 8
+#endif
+constexpr int kMergeWidePieces = PKV_MERGE_WIDE_PIECES;  // expected pieces per segment
 constexpr int kMergeBatch = 8;
 
-template <typename T, int kTT>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const DecodeArgs a) {
+#ifndef PKV_MERGE_NARROW_CTAS
+#define PKV_MERGE_NARROW_CTAS 1
+#endif
+#ifndef PKV_MERGE_WIDE_CTAS
+#define PKV_MERGE_WIDE_CTAS 3
+#endif
+// CTAs per SM the register budget allows (merge CTAs start as streaming CTAs
+// leave their SMs, so a merge grid that fits in one wave drains quickest)
+constexpr int kMergeNarrowCtas = PKV_MERGE_NARROW_CTAS;
+constexpr int kMergeWideCtas = PKV_MERGE_WIDE_CTAS;
+
+template <typename T, int kTT, bool kWide>
+__global__ void __launch_bounds__((kWide ? kMergeWideWarps : kMergeWarps) * 32,
+                                  kWide ? kMergeWideCtas : kMergeNarrowCtas)
+    merge_stream_kernel(const DecodeArgs a) {
     const int g = a.group;
     const int H = a.num_kv_heads;
     const int S = a.num_seqs;
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    const int warp = threadIdx.x >> 5;
+    constexpr int kWpi = kWide ? kMergeWideWarps : 1;  // warps per item
+    const int sub = kWide ? warp : 0;                  // this warp's place among them
+    // every early exit below depends on the item alone: uniform over a wide CTA
+    const int64_t item = kWide ? static_cast<int64_t>(blockIdx.x)
+                               : static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
     if (item >= static_cast<int64_t>(S) * H * g) return;
     const int lane = threadIdx.x & 31;
     const int r = static_cast<int>(item % g);
@@ -363,8 +392,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
         (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * g + r) * kHeadDim +
         lane * 4);
     if (nt == 0) {  // empty sequence: zero output
-        ocol[0] = 0u;
-        ocol[1] = 0u;
+        if (sub == 0) {
+            ocol[0] = 0u;
+            ocol[1] = 0u;
+        }
         return;
     }
     const int64_t per = (total_tiles + a.num_warps - 1) / a.num_warps;
@@ -377,7 +408,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
 
     float big = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = 0; base < np; base += kMergeBatch) {
+    for (int base = sub * kMergeBatch; base < np; base += kWpi * kMergeBatch) {
         float m[kMergeBatch], l[kMergeBatch];
         float4 v[kMergeBatch];
 #pragma unroll
@@ -403,6 +434,36 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_stream_kernel(const De
             big = nb;
         }
     }
+    if constexpr (kWide) {
+        // dynamic shared memory: acc [warps][32] float4, then max and sum [warps]
+        extern __shared__ float4 merge_smem[];
+        float4(*s_acc)[32] = reinterpret_cast<float4(*)[32]>(merge_smem);
+        float* s_big = reinterpret_cast<float*>(merge_smem + kMergeWideWarps * 32);
+        float* s_den = s_big + kMergeWideWarps;
+        if (lane == 0) {
+            s_big[warp] = big;
+            s_den[warp] = den;
+        }
+        s_acc[warp][lane] = acc;
+        __syncthreads();
+        if (warp != 0) return;
+        big = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kMergeWideWarps; ++w) big = fmaxf(big, s_big[w]);
+        den = 0.f;
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kMergeWideWarps; ++w) {
+            if (s_big[w] == -INFINITY) continue;  // no pieces, or none with a token
+            const float sc = ex2(s_big[w] - big);
+            const float4 v = s_acc[w][lane];
+            den += s_den[w] * sc;
+            acc.x += v.x * sc;
+            acc.y += v.y * sc;
+            acc.z += v.z * sc;
+            acc.w += v.w * sc;
+        }
+    }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     ocol[0] = Mma<T>::pack(acc.x * inv, acc.y * inv);
     ocol[1] = Mma<T>::pack(acc.z * inv, acc.w * inv);
@@ -417,7 +478,7 @@ constexpr size_t stream_smem_bytes(int num_seqs) {
 
 template <typename Policy, int BS>
 cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_map,
-                                const DecodeArgs& a, int ctas, cudaStream_t stream) {
+                                const DecodeArgs& a, int ctas, int sms, cudaStream_t stream) {
     using T = typename Policy::Scalar;
     constexpr bool kFp8 = Policy::kFp8;
     const size_t smem = stream_smem_bytes<kFp8, Policy::kWarps>(a.num_seqs);
@@ -427,22 +488,30 @@ cudaError_t launch_stream_typed(const CUtensorMap& k_map, const CUtensorMap& v_m
     err = launch_pdl(kernel, dim3(ctas), dim3(Policy::kWarps * 32), smem, stream, k_map, v_map, a);
     if (err != cudaSuccess) return err;
     const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.group;
+    constexpr int kTT = StreamLayout<kFp8, Policy::kWarps>::kTileTokens;
+    // The wide form for about kMergeWidePieces or more pieces per segment,
+    // when its grid fits in one wave.
+    if (a.num_warps >= kMergeWidePieces * static_cast<int64_t>(a.num_seqs) * a.num_kv_heads &&
+        items <= static_cast<int64_t>(kMergeWideCtas) * sms) {
+        constexpr size_t kWideSmem = kMergeWideWarps * (32 * sizeof(float4) + 2 * sizeof(float));
+        return launch_pdl(merge_stream_kernel<T, kTT, true>, dim3(static_cast<unsigned>(items)),
+                          dim3(kMergeWideWarps * 32), kWideSmem, stream, a);
+    }
     const int64_t blocks = (items + kMergeWarps - 1) / kMergeWarps;
-    return launch_pdl(merge_stream_kernel<T, StreamLayout<kFp8, Policy::kWarps>::kTileTokens>,
-                      dim3(static_cast<unsigned>(blocks)),
+    return launch_pdl(merge_stream_kernel<T, kTT, false>, dim3(static_cast<unsigned>(blocks)),
                       dim3(kMergeWarps * 32), 0, stream, a);
 }
 
 template <typename Policy>
 cudaError_t launch_stream_block(const CUtensorMap& k_map, const CUtensorMap& v_map,
-                                const DecodeArgs& a, int block_size, int ctas,
+                                const DecodeArgs& a, int block_size, int ctas, int sms,
                                 cudaStream_t stream) {
     switch (block_size) {
-        case 8: return launch_stream_typed<Policy, 8>(k_map, v_map, a, ctas, stream);
-        case 16: return launch_stream_typed<Policy, 16>(k_map, v_map, a, ctas, stream);
-        case 32: return launch_stream_typed<Policy, 32>(k_map, v_map, a, ctas, stream);
-        case 64: return launch_stream_typed<Policy, 64>(k_map, v_map, a, ctas, stream);
-        default: return launch_stream_typed<Policy, 128>(k_map, v_map, a, ctas, stream);
+        case 8: return launch_stream_typed<Policy, 8>(k_map, v_map, a, ctas, sms, stream);
+        case 16: return launch_stream_typed<Policy, 16>(k_map, v_map, a, ctas, sms, stream);
+        case 32: return launch_stream_typed<Policy, 32>(k_map, v_map, a, ctas, sms, stream);
+        case 64: return launch_stream_typed<Policy, 64>(k_map, v_map, a, ctas, sms, stream);
+        default: return launch_stream_typed<Policy, 128>(k_map, v_map, a, ctas, sms, stream);
     }
 }
 
@@ -477,8 +546,9 @@ cudaError_t launch_stream(const CUtensorMap& k_map, const CUtensorMap& v_map, De
     a.ws_l = a.ws_m + rows;
     return dtype == PKV_BF16
                ? launch_stream_block<Policy<__nv_bfloat16>>(k_map, v_map, a, block_size, (int)ctas,
-                                                            stream)
-               : launch_stream_block<Policy<__half>>(k_map, v_map, a, block_size, (int)ctas, stream);
+                                                            sms, stream)
+               : launch_stream_block<Policy<__half>>(k_map, v_map, a, block_size, (int)ctas, sms,
+                                                     stream);
 }
 
 }  // namespace

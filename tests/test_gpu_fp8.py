@@ -158,6 +158,13 @@ def test_long_sequences_cut_across_warps():
     fp8_step_parity(step, what="long fp8")
 
 
+def test_long_sequences_with_empty_ones_cut_across_warps():
+    """Few long segments over many warps, with an empty and a one-token sequence."""
+    step = _custom([15000, 0, 1, 7000], 16, 2, 16, "float16", seed=74)
+    step.seq_lens[1] = 0  # nothing attended for sequence 1
+    fp8_step_parity(step, what="long and empty")
+
+
 @pytest.mark.parametrize("hq,hkv", [(16, 1), (16, 16), (32, 16), (64, 8), (48, 6)])
 def test_group_sizes(hq, hkv):
     step = _custom([1, 15, 16, 17, 300, 1000], hq, hkv, 16, "bfloat16", seed=65 + hq + hkv)

@@ -292,6 +292,16 @@ def test_stream_single_long_sequence_many_partials():
     _full_step_parity(step, partition_sizes=(0,))
 
 
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
+def test_stream_wide_merge_with_empty_and_short_sequences(dtype):
+    """Few long segments over many warps (one CTA merges each segment and query
+    head), mixed with empty, one-token and one-tile sequences."""
+    context = [20000, 0, 4, 0, 12000, 299, 15]
+    step = _custom(context, 8, 2, 16, dtype, seed=34)
+    step.seq_lens[3] = 0  # an empty sequence between two long ones
+    _full_step_parity(step, partition_sizes=(0,))
+
+
 def test_stream_workspace_reuse_with_leftover_contents():
     """A workspace full of unrelated bytes, reused across shapes, gives correct outputs."""
     a = _custom([3000, 900, 4000, 17], 32, 8, 16, "bfloat16", seed=40)

@@ -297,12 +297,16 @@ def time_calls(call, reps=200, warmup=10):
 L2_FLUSH_BYTES = 512 << 20  # written between calls whose inputs could stay in the 129 MB L2
 
 
-def time_calls_graph(call, per_graph=20, replays=10, flush=False):
+def time_calls_graph(call, per_graph=20, replays=10, flush=False, clean_l2=True):
     """Average device time of one call replayed from a CUDA graph of `per_graph`
     calls: no host launch cost, as a serving loop that captures its decode
     step would issue it (median over replays, CUDA events).  With `flush`,
-    every call follows a 512 MiB write that evicts L2, and the time of a
-    graph of the writes alone is subtracted."""
+    every call follows a 512 MiB write that evicts L2 and the time of a graph
+    of the flushes alone is subtracted.  With `clean_l2` the write is followed
+    by a read of the same buffer, which leaves L2 holding clean lines, so a
+    call that mostly reads does not pay the write-back of the flush.  Calls
+    that mostly write take `clean_l2=False`: their own writes would otherwise
+    sit in a clean L2 and be written back during the next (subtracted) flush."""
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -318,6 +322,8 @@ def time_calls_graph(call, per_graph=20, replays=10, flush=False):
             for _ in range(per_graph):
                 if scratch is not None:
                     scratch.fill_(1)
+                    if clean_l2:
+                        scratch.view(torch.int32).amax()
                 if with_call:
                     call()
         graph.replay()
@@ -467,20 +473,35 @@ def scenario_steps(pkv, device, sc, steps, physical_blocks):
                                        outs[int(p["q"].shape[0])],
                                        max_seq_len=p["max_seq_len"], workspace=ws)
 
-    run_all()  # warm-up pass (also replays the copies and writes once)
-    # restore the initial pools so the timed pass replays the same work
-    k_cache.copy_(sc.k_cache.to(device))
-    v_cache.copy_(sc.v_cache.to(device))
+    def restore():  # the initial pools, so every timed pass replays the same work
+        k_cache.copy_(sc.k_cache.to(device))
+        v_cache.copy_(sc.v_cache.to(device))
+        torch.cuda.synchronize()
+
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    run_all()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+
+    def timed(fn):
+        restore()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    run_all()  # warm-up pass (also replays the copies and writes once)
+    eager_ms = timed(run_all)
+    # the same steps captured once in a CUDA graph: device time without the
+    # host's per-call cost, as a serving loop that captures its steps runs them
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_all()
+    graph.replay()  # first replay off the clock
+    ms = timed(graph.replay)
     hbm, _ = measured_peaks()
     return {"ms_per_step": round(ms / steps, 4),
+            "timing": "one CUDA-graph replay of all steps (the pools restored before it)",
+            "ms_per_step_eager": round(eager_ms / steps, 4),
             "decode_tokens_per_s": round(tokens / (ms * 1e-3), 1),
             "cow_copies": copies,
             "logical_gbs": round(logical / (ms * 1e-3) / 1e9, 1),
@@ -678,7 +699,7 @@ def writes_throughput(pkv, W, device, n_pairs=2000):
                         "(K and V read and written)"),
     }
     for name, (call, nbytes, what) in cases.items():
-        ms = time_calls_graph(call, flush=nbytes < L2_FLUSH_BYTES)
+        ms = time_calls_graph(call, flush=nbytes < L2_FLUSH_BYTES, clean_l2=False)
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[name] = {"workload": what, "us": round(ms * 1e3, 2), "bytes": int(nbytes),
                      "gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / hbm, 4),

@@ -46,7 +46,8 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 SINGLE_WORKLOADS = ("tiny", "opt13b_like", "long_context", "long_context_fp8", "prefix_sharing",
-                    "prefix_sharing_cow", "swap", "writes", "beam_search", "decode_shapes")
+                    "prefix_sharing_cow", "swap", "writes", "beam_search", "decode_shapes",
+                    "prefill_shapes")
 
 
 def parse_args():
@@ -594,9 +595,9 @@ def measured_bf16_tflops():
         return 1900.0, "fallback"
 
 
-def measure_prefill(pkv, W, device, reps=20):
-    """Causal paged prefill of the prefill batch (attention alone, after kv_write)."""
-    st = W.prefill_batch()
+def time_prefill(pkv, st, device, reps=20):
+    """Device ms per causal paged prefill call of step `st` (attention alone,
+    after its kv_write), CUDA events around `reps` back-to-back calls."""
     dev = {k: getattr(st, k).to(device) for k in
            ("q", "cu_q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
             "k_cache", "v_cache")}
@@ -618,12 +619,18 @@ def measure_prefill(pkv, W, device, reps=20):
         call()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    del dev, out
+    torch.cuda.empty_cache()
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_prefill(pkv, W, device, reps=20):
+    """Causal paged prefill of the prefill batch (attention alone, after kv_write)."""
+    st = W.prefill_batch()
+    ms = time_prefill(pkv, st, device, reps)
     flops = st.causal_flops()
     peak, kind = measured_bf16_tflops()
     tflops = flops / (ms * 1e-3) / 1e12
-    del dev
-    torch.cuda.empty_cache()
     return {"workload": f"{st.num_seqs} prompts of 512..2048 tokens (total {int(st.q.shape[0])}), "
                         "causal, 32 q / 8 kv heads, bf16, block 16",
             "attention_ms": round(ms, 4), "useful_tflops": round(tflops, 1),
@@ -631,6 +638,37 @@ def measure_prefill(pkv, W, device, reps=20):
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "peak_kind": f"{kind} bf16 dense (burst)"},
             "prompt_tokens_per_s": round(int(st.q.shape[0]) / (ms * 1e-3), 1)}
+
+
+def prefill_shapes(pkv, W, device):
+    """Causal paged prefill on other shapes (32 q / 8 kv heads, block 16)."""
+    batch = W.prefill_batch()
+    q_lens = (batch.cu_q[1:] - batch.cu_q[:-1]).tolist()
+    g = torch.Generator().manual_seed(13)
+    mixed_ctx = torch.randint(100, 600, (253,), generator=g).tolist()
+    mixed_q = [1] * 253
+    for i, n in ((7, 1500), (100, 700), (200, 1100)):  # three prompts among one-token steps
+        mixed_ctx[i], mixed_q[i] = 0, n
+    shapes = {
+        "batch_fp16": ("the prefill batch's prompts in fp16", [0] * len(q_lens), q_lens,
+                       "float16"),
+        "uniform_16x2048": ("16 prompts of 2048 tokens", [0] * 16, [2048] * 16, "bfloat16"),
+        "ctx4096_q512x16": ("16 x 512 queries after 4096 cached tokens", [4096] * 16, [512] * 16,
+                            "bfloat16"),
+        "short_256x128": ("256 prompts of 128 tokens", [0] * 256, [128] * 256, "bfloat16"),
+        "mixed_253": ("250 one-token steps (100..599 cached) and prompts of 1500, 700, 1100",
+                      mixed_ctx, mixed_q, "bfloat16"),
+    }
+    peak, kind = measured_bf16_tflops()
+    res = {}
+    for i, (name, (what, ctx, ql, dtype)) in enumerate(shapes.items()):
+        st = W.build_prefill_step(name, ctx, ql, 32, 8, 16, dtype, seed=300 + i)
+        ms = time_prefill(pkv, st, device)
+        tflops = st.causal_flops() / (ms * 1e-3) / 1e12
+        res[name] = {"workload": f"{what}, {dtype}", "attention_ms": round(ms, 4),
+                     "useful_tflops": round(tflops, 1),
+                     "frac_of_measured_bf16": round(tflops / peak, 4)}
+    return res
 
 
 def other_workloads(pkv, W, device, all_configs):
@@ -670,6 +708,7 @@ def other_workloads(pkv, W, device, all_configs):
         extra["prefix_sharing_cow"] = prefix_sharing_steps(pkv, W, device, 1040)
         extra["beam_search"] = beam_search_steps(pkv, W, device)
         extra["decode_shapes"] = decode_shapes(pkv, W, device)
+        extra["prefill_shapes"] = prefill_shapes(pkv, W, device)
     return extra
 
 
@@ -751,6 +790,8 @@ def single_workload(pkv, W, device, name):
         return beam_search_steps(pkv, W, device)
     if name == "decode_shapes":
         return decode_shapes(pkv, W, device)
+    if name == "prefill_shapes":
+        return prefill_shapes(pkv, W, device)
     return prefix_sharing_steps(pkv, W, device, 1040 if name == "prefix_sharing_cow" else 1024)
 
 

@@ -25,9 +25,9 @@
 //              warp 2 for B: for each key tile S = Q K^T (Q and K from shared
 //              memory), then O += P V of the previous key tile (P read from
 //              tensor memory, V from shared memory).  With bf16 inputs P is
-//              split into a bf16 high part and the low part of the remainder
-//              (two MMAs per step, so the weights keep about 16 significant
-//              bits); with fp16 inputs P is one binary16 value (11 bits).  With an
+//              split into a bf16 high part (its top 16 bits) and the rounded
+//              remainder (two MMAs per step, so the weights keep about 16
+//              significant bits); with fp16 inputs P is one binary16 value (11 bits).  With an
 //              issuer per tile neither tile's S waits behind the other's
 //              softmax;
 //   warps 3-6  softmax of Q tile A, warps 7-10 of Q tile B, one thread per row
@@ -71,7 +71,8 @@ constexpr uint32_t kOCol = 128;
 constexpr float kRescaleLog2 = 8.f;
 
 // P's 16-bit parts: bf16 keeps 8 significant bits, so P is split into a high
-// part and the low part of the remainder; binary16 keeps 11 and goes whole.
+// part (the top 16 bits of the fp32 weight, a bf16 value exactly) and the
+// exact remainder rounded to bf16; binary16 keeps 11 and goes whole.
 template <typename T>
 constexpr int kPParts = std::is_same<T, __nv_bfloat16>::value ? 2 : 1;
 
@@ -93,7 +94,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // evaluated as one fused operation, without the product's rounding, so they
 // are used only where no multiply feeds an add: the scale before the max, the
 // exponent argument (an explicit fma), the sums of weights and the low part
-// of P (a subtract of unpacked values).
+// of P (the weight minus its bit-truncated high part).
 __device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b) {
     asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
         "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
@@ -632,20 +633,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     weights(base);
                 }
                 uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    pw[e] = Mma<T>::pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                tmem_st32(sp_addr, pw);
-                if constexpr (kPParts<T> == 2) {  // the low part of the remainder beside it
+                if constexpr (kPParts<T> == 2) {
+                    // High part: the weight cut to its top 16 bits, a bf16 value
+                    // exactly, paired by one byte permute.  Low part: the exact
+                    // fp32 remainder (below 2^-7 of the weight), rounded to bf16,
+                    // so the pair carries the weight within 2^-16 of it.  This takes
+                    // one conversion per pair instead of two plus an unpack.
+                    uint32_t lw[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float2 back = Mma<T>::unpack(pw[e]);
+                        const uint32_t h0 = v[2 * e] & 0xFFFF0000u, h1 = v[2 * e + 1] & 0xFFFF0000u;
+                        pw[e] = __byte_perm(v[2 * e], v[2 * e + 1], 0x7632);
                         float r0, r1;
                         sub2(r0, r1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]),
-                             back.x, back.y);
-                        pw[e] = Mma<T>::pack(r0, r1);
+                             __uint_as_float(h0), __uint_as_float(h1));
+                        lw[e] = Mma<T>::pack(r0, r1);
                     }
-                    tmem_st32(sp_addr + 32, pw);
+                    tmem_st32(sp_addr, pw);
+                    tmem_st32(sp_addr + 32, lw);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        pw[e] = Mma<T>::pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                    tmem_st32(sp_addr, pw);
                 }
                 tmem_st_wait();
                 l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));

@@ -748,6 +748,11 @@ def writes_throughput(pkv, W, device, n_pairs=2000):
     return res
 
 
+# what the --only lines of the workloads that are not decode attention measure
+ONLY_METRICS = {"swap": "block swap GB/s between a device pool and a page-locked host pool",
+                "writes": "kv_write / copy_blocks GB/s",
+                "prefill_shapes": "causal paged prefill useful TFLOP/s"}
+
 # (sequences, tokens each): from one sequence to a few dozen, 32 q / 8 kv heads
 DECODE_SHAPES = ((1, 2048), (4, 4096), (1, 32768), (16, 2048), (32, 1024))
 
@@ -1107,7 +1112,8 @@ def main():
             torch.cuda.set_device(device)
             rec = single_workload(pkv, W, device, args.only)
             if rank == 0:
-                print(json.dumps(dict(metric=METRIC, only=args.only, **rec)), flush=True)
+                print(json.dumps(dict(metric=ONLY_METRICS.get(args.only, METRIC), only=args.only,
+                                      **rec)), flush=True)
         elif args.only == "prefill":
             import paged_kv_cache_242_gb300 as pkv
             from paged_kv_cache_242_gb300 import workloads as W

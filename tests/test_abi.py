@@ -215,3 +215,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIBRARY", str(tmp_path / "absent.so"))
     with pytest.raises(_lib.PKVError):
         _lib.load()
+
+
+def test_build_flags_decide_whether_the_library_is_current(monkeypatch, tmp_path):
+    """A library built with other nvcc options than the current ones is rebuilt."""
+    lib_path = tmp_path / "libpkv.so"
+    monkeypatch.setattr(build, "BUILD_DIR", str(tmp_path))
+    monkeypatch.setattr(build, "LIBRARY", str(lib_path))
+    monkeypatch.delenv("PKV_NVCC_EXTRA_FLAGS", raising=False)
+    assert not build.up_to_date()  # no library
+    lib_path.write_bytes(b"")
+    future = max(os.path.getmtime(p) for p in build._inputs()) + 10
+    os.utime(lib_path, (future, future))
+    assert not build.up_to_date()  # no record of its flags
+    (tmp_path / "flags.txt").write_text(" ".join(build._flags()))
+    assert build.up_to_date()
+    monkeypatch.setenv("PKV_NVCC_EXTRA_FLAGS", "-DPKV_MERGE_WIDE_PIECES=16")
+    assert not build.up_to_date()  # other definitions
+    (tmp_path / "flags.txt").write_text(" ".join(build._flags()))
+    assert build.up_to_date()
